@@ -1,0 +1,45 @@
+"""The five synthetic workloads of the projection hot path.
+
+Shapes follow the DiT block of the pages: hidden 5120, MLP width 13824, fused
+QKV 5120 -> 15360 with LoRA rank/alpha 384, attention-out 5120 -> 5120, fused
+gate/up 5120 -> 27648 with SiLU*up, down 13824 -> 5120, all rank/alpha 128
+(TURBO.md, h3-blackwell-runtime, "Implementation"; MiniMax-H3 Ultra Fast README,
+"Active optimization stack" rows "Attention projections" and "MLP").  The
+packed sequence is ragged: S = 37726 for a 16-token prompt, 37728 for an
+18-token one (MiniMax-H3 AoTI packages, "What is here").
+"""
+from __future__ import annotations
+
+HIDDEN = 5120
+MLP = 13824
+
+# name, K, N, rank, SiLU*up epilogue
+BLOCK_PROJECTIONS = (
+    ("qkv", HIDDEN, 3 * HIDDEN, 384, False),
+    ("attn_out", HIDDEN, HIDDEN, 128, False),
+    ("gate_up", HIDDEN, 2 * MLP, 128, True),
+    ("down", MLP, HIDDEN, 128, False),
+)
+
+TINY = dict(name="tiny", M=200, K=256, N=384, rank=16, seed=0, law="normal", outlier_frac=0.0)
+QKV = dict(name="qkv_9437", M=9437, K=HIDDEN, N=3 * HIDDEN, rank=384, seed=1, law="normal",
+           outlier_frac=0.01)
+BLOCK_S = 37726
+BLOCK_SEED = 2
+SWITCH_S = 37728
+SWITCH_SEED = 4
+SWITCH_ADAPTER_SEEDS = (41, 42)
+SWITCH_STRENGTHS = (0.0, 0.5, 1.0)
+SWEEP_M = (1024, 4096, 16384, 37726, 65536)
+SWEEP_SEEDS = (3, 4, 5, 6, 7)
+
+
+def block_flops(S, with_lora=True):
+    """Algorithmic FLOPs of the four block projections at sequence length S:
+    base ``2 S K N`` plus LoRA ``2 S K r + 2 S r N`` per projection."""
+    total = 0
+    for _, K, N, r, _ in BLOCK_PROJECTIONS:
+        total += 2 * S * K * N
+        if with_lora:
+            total += 2 * S * K * r + 2 * S * r * N
+    return total
