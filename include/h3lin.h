@@ -1,0 +1,166 @@
+/*
+ * h3lin — dynamic-LoRA NVFP4 linear for GB300 (sm_103a): the C ABI.
+ *
+ * The operation (TURBO.md, h3-blackwell-runtime, section "Implementation"):
+ *
+ *     out = NVFP4_base(x * pre_quant_scale) + strength * (alpha / rank) * B(A(x))
+ *
+ * The NVFP4 base branch quantises the pre-scaled activation at run time
+ * ("dynamic NVFP4 activation quantization", MiniMax-H3 Ultra Fast README,
+ * section "Kernel path", item 1) and multiplies it with the packed NVFP4
+ * weight on the FP4 tensor cores.  The BF16 LoRA branch receives the ORIGINAL
+ * activation and is never merged into the packed weight (TURBO.md,
+ * "Implementation").  The fused gate/up projection applies silu(gate) * up in
+ * place (Ultra Fast README, table "Active optimization stack", row MLP).
+ *
+ * NVFP4 encoding used throughout (the format's public definition):
+ *   codes   E2M1, two per byte, element 2j in bits 0-3, element 2j+1 in 4-7,
+ *           row-major [rows, K/2];
+ *   scales  one E4M3 scale per 16 elements along K, stored in the NATIVE
+ *           layout: 512-byte atoms covering 128 rows x 64 columns, atoms
+ *           ordered [rows/128][K/64]; inside an atom the scale of row r,
+ *           16-block j sits at byte (r % 32) * 16 + (r / 32) * 4 + j
+ *           (rows padded to a multiple of 128; padded rows hold scale 0);
+ *   tensor  one FP32 scale per tensor, amax / 2688 (1 when that is zero),
+ *           kept in device memory.
+ *
+ * Conventions (all entry points):
+ *   - Pointers marked "device" are CUDA device pointers; the library never
+ *     allocates or frees memory.  The caller owns every buffer.
+ *   - Work is enqueued asynchronously on `stream` (0 = legacy default stream);
+ *     no call synchronises except h3lin_read_status.
+ *   - Arguments are validated on the host BEFORE anything is enqueued; on any
+ *     error the call returns a non-zero status and enqueues nothing.
+ *   - Calls keep no state between them (no caches keyed by pointer); the
+ *     adapter is chosen per call.  A workspace must not be used by two calls
+ *     that may run concurrently.
+ *   - Kernels never trap: every device-side wait is bounded; on expiry the
+ *     kernel records H3LIN_E_TIMEOUT in the workspace status word and returns.
+ *
+ * Shape rules: M >= 1; K % 64 == 0; N % 128 == 0 (SiLU*up: N % 256 == 0);
+ * rank % 16 == 0 and 16 <= rank <= 256, or rank % 32 == 0 and rank <= 512;
+ * x, codes, scales, out, A, B 16-byte aligned; rows and K below 2^31.
+ */
+#ifndef H3LIN_H
+#define H3LIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define H3LIN_ABI_VERSION 1
+
+typedef int32_t h3lin_status;
+#define H3LIN_OK            0
+#define H3LIN_E_INVALID     1  /* null pointer, unknown enum, non-finite scalar      */
+#define H3LIN_E_SHAPE       2  /* a shape rule above is violated                      */
+#define H3LIN_E_ALIGN       3  /* a pointer is not 16-byte aligned                    */
+#define H3LIN_E_WORKSPACE   4  /* workspace too small                                 */
+#define H3LIN_E_CUDA        5  /* CUDA runtime error while enqueueing / no device     */
+#define H3LIN_E_TIMEOUT     6  /* device-side bounded wait expired (device status)    */
+#define H3LIN_E_UNSUPPORTED 7  /* device is not compute capability 10.x (tcgen05)     */
+
+/* Epilogues of h3lin_forward. */
+#define H3LIN_EPI_NONE      0  /* out[M, N] = y                                       */
+#define H3LIN_EPI_SILU_MUL  1  /* y = [gate | up] (N = 2 * Nh); out[M, Nh] = silu(gate) * up */
+
+/* A packed NVFP4 weight W[N, K] (as written by h3lin_pack_weight).  POD,
+ * caller-owned; all three pointers are device pointers. */
+typedef struct {
+    const void*  codes;         /* u8 [N, K/2]                                      */
+    const void*  scales;        /* u8, native layout, h3lin_scales_bytes(N, K) bytes */
+    const float* tensor_scale;  /* 1 float                                           */
+    int64_t      N, K;
+} h3lin_weight;
+
+/* One resident LoRA adapter for one projection.  POD, caller-owned; A and B
+ * are device pointers to row-major bf16. */
+typedef struct {
+    const void* A;      /* bf16 [rank, K]: down projection, applied to the original x */
+    const void* B;      /* bf16 [N, rank]: up projection (gate/up: rows [gate; up])   */
+    int32_t     rank;
+    float       alpha;  /* the adapter's alpha; the branch is scaled by alpha / rank  */
+} h3lin_adapter;
+
+/* ------------------------------------------------------------------ sizes */
+/* Bytes of the packed codes / native scales of a [rows, K] NVFP4 tensor
+ * (0 when the shape is invalid). */
+size_t h3lin_codes_bytes(int64_t rows, int64_t K);
+size_t h3lin_scales_bytes(int64_t rows, int64_t K);
+/* Workspace of h3lin_quantize_act / h3lin_pack_weight (status word, tensor
+ * scale, per-CTA amax partials). */
+size_t h3lin_quant_workspace_bytes(void);
+/* Workspace of h3lin_forward for activations of up to M rows, in-features K,
+ * out-features N (before the epilogue) and adapters of rank up to max_rank
+ * (0 = no adapter will ever be passed).  Holds the quantised activation, the
+ * LoRA intermediate A(x), the scaled copy of B and the quantiser header. */
+size_t h3lin_forward_workspace_bytes(int64_t M, int64_t K, int64_t N, int32_t max_rank);
+
+/* Zero the status word and header of a workspace (enqueued on `stream`).
+ * Call once after allocating a workspace, and after reading an error. */
+h3lin_status h3lin_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* --------------------------------------------------------------- quantiser */
+/* Dynamic NVFP4 quantisation of an activation (Ultra Fast README, "Kernel
+ * path", item 1) with the checkpoint's per-input-channel pre_quant_scale
+ * (TURBO.md, "Implementation"):  v = x * s in FP32, ts = amax|v| / 2688,
+ * per-16 E4M3 scale = RNE_sat(blockamax / (6 ts)), codes = RNE_sat(v / (scale ts))
+ * (the division taken as v * (1 / (scale * ts))).
+ *   x                device bf16 [M, K] row-major
+ *   pre_quant_scale  device fp32 [K], or NULL for all ones
+ *   codes            device u8 [M, K/2]                (output)
+ *   scales           device u8 h3lin_scales_bytes(M,K) (output, native layout)
+ *   tensor_scale     device fp32 [1]                   (output)
+ *   workspace        device, >= h3lin_quant_workspace_bytes(), initialised once
+ * Two kernels: an amax pass and the quantise pass. */
+h3lin_status h3lin_quantize_act(const void* x, int64_t M, int64_t K, const float* pre_quant_scale,
+                                void* codes, void* scales, float* tensor_scale,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* One-time packing of a bf16 weight W[N, K] (row-major) into NVFP4: the same
+ * rules with s = 1 (TURBO.md, "Implementation": the packed NVFP4 base).  For
+ * the fused gate/up projection pass W = [gate; up] (N = 2 * Nh rows). */
+h3lin_status h3lin_pack_weight(const void* w, int64_t N, int64_t K,
+                               void* codes, void* scales, float* tensor_scale,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ----------------------------------------------------------------- forward */
+/* One projection:  out = NVFP4_base(x * s) + strength * (alpha/rank) * B(A(x)),
+ * followed by the epilogue.
+ *   x                device bf16 [M, K] row-major (M ragged: no padding needed)
+ *   pre_quant_scale  device fp32 [K] or NULL
+ *   weight           packed weight with weight->K == K
+ *   epilogue         H3LIN_EPI_NONE or H3LIN_EPI_SILU_MUL
+ *   adapter          NULL selects the base path; otherwise A [rank, K],
+ *                    B [weight->N, rank].  strength == 0 also selects the base
+ *                    path, whose output is bit-identical to adapter == NULL
+ *                    (TURBO.md, "Validation": disabled exactness).
+ *   strength         finite float
+ *   out              device bf16 [M, N] (SiLU*up: [M, N/2]); rows >= M untouched
+ *   workspace        device, >= h3lin_forward_workspace_bytes(M, K, N, rank),
+ *                    initialised once with h3lin_workspace_init
+ * Kernels (stream order): amax pass (fused with A(x) when the adapter is
+ * active), quantise pass (also writes the scaled copy of B), then the FP4
+ * GEMM whose TMEM accumulator also receives B(A(x)) before the epilogue. */
+h3lin_status h3lin_forward(const void* x, int64_t M, const float* pre_quant_scale,
+                           const h3lin_weight* weight, int32_t epilogue,
+                           const h3lin_adapter* adapter, float strength,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------ status */
+/* Synchronises `stream`, then reads the workspace's sticky device status word
+ * (H3LIN_OK or H3LIN_E_TIMEOUT) into *device_status.  Returns H3LIN_E_CUDA if
+ * the stream reported an error. */
+h3lin_status h3lin_read_status(const void* workspace, cudaStream_t stream, int32_t* device_status);
+const char*  h3lin_status_string(h3lin_status status);
+int32_t      h3lin_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3LIN_H */

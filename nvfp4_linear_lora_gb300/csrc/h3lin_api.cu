@@ -1,0 +1,305 @@
+// C ABI of the dynamic-LoRA NVFP4 linear: argument validation (on the host,
+// before anything is enqueued), workspace layout, TMA tensor maps and the
+// kernel sequence.  See include/h3lin.h for the contract of every call.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "h3lin_internal.h"
+
+namespace h3lin {
+namespace {
+
+constexpr int64_t kMaxDim = int64_t(1) << 30;   // rows, N
+constexpr int64_t kMaxK = int64_t(1) << 17;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- device
+struct DeviceInfo {
+  int sm_count = 0;
+  int major = 0, minor = 0;
+};
+
+h3lin_status device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return H3LIN_E_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && have[dev]) {
+    *out = cache[dev];
+    return H3LIN_OK;
+  }
+  DeviceInfo d;
+  if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return H3LIN_E_CUDA;
+  }
+  if (dev < 64) {
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *out = d;
+  return H3LIN_OK;
+}
+
+h3lin_status require_device(DeviceInfo* d) {
+  h3lin_status s = device_info(d);
+  if (s != H3LIN_OK) return s;
+  if (!(d->major == 10 && d->minor == 3)) return H3LIN_E_UNSUPPORTED;  // kernels are built for sm_103a
+  return H3LIN_OK;
+}
+
+// ----------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Row-major 2-D tensor [rows, inner] with a 128-byte-swizzled box.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool rank_ok(int64_t r) {
+  if (r < 16) return false;
+  if (r <= 256) return r % 16 == 0;
+  return r <= 512 && r % 32 == 0;
+}
+
+struct ForwardLayout {
+  size_t codes, scales, u, b, total;
+};
+ForwardLayout forward_layout(int64_t M, int64_t K, int64_t N, int64_t rank) {
+  ForwardLayout L;
+  const int64_t mpad = (M + 127) / 128 * 128;
+  size_t off = align_up(kHeaderBytes, kRegionAlign);
+  L.codes = off;
+  off = align_up(off + size_t(M) * size_t(K / 2), kRegionAlign);
+  L.scales = off;
+  off = align_up(off + size_t(mpad) * size_t(K / 16), kRegionAlign);
+  L.u = off;
+  off = align_up(off + size_t(M) * size_t(rank) * 2, kRegionAlign);
+  L.b = off;
+  off = align_up(off + size_t(N) * size_t(rank) * 2, kRegionAlign);
+  L.total = off;
+  return L;
+}
+
+h3lin_status quantize_impl(const void* x, int64_t M, int64_t K, const float* pqs, void* codes, void* scales,
+                           float* ts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!x || !codes || !scales || !ts || !ws) return H3LIN_E_INVALID;
+  if (M < 1 || M > kMaxDim || K < 64 || K > kMaxK || K % 64 != 0) return H3LIN_E_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(ws) || (pqs && !aligned16(pqs)) ||
+      (reinterpret_cast<uintptr_t>(ts) & 3u))
+    return H3LIN_E_ALIGN;
+  if (ws_bytes < kHeaderBytes) return H3LIN_E_WORKSPACE;
+  DeviceInfo d;
+  h3lin_status s = require_device(&d);
+  if (s != H3LIN_OK) return s;
+  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kPartialsOffset);
+  const RowPlan plan = plan_rows(M, K, d.sm_count);
+  if (launch_amax(x, int(M), int(K), pqs, partials, plan, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  if (launch_quant(x, int(M), int(K), pqs, partials, plan.blocks, codes, scales, ts, plan, nullptr, nullptr, 0,
+                   0.0f, nullptr, stream) != cudaSuccess)
+    return H3LIN_E_CUDA;
+  return H3LIN_OK;
+}
+
+}  // namespace
+}  // namespace h3lin
+
+using namespace h3lin;
+
+extern "C" {
+
+int32_t h3lin_abi_version(void) { return H3LIN_ABI_VERSION; }
+
+const char* h3lin_status_string(h3lin_status s) {
+  switch (s) {
+    case H3LIN_OK: return "ok";
+    case H3LIN_E_INVALID: return "invalid argument (null pointer, unknown enum or non-finite scalar)";
+    case H3LIN_E_SHAPE: return "shape rule violated";
+    case H3LIN_E_ALIGN: return "pointer not 16-byte aligned";
+    case H3LIN_E_WORKSPACE: return "workspace too small";
+    case H3LIN_E_CUDA: return "CUDA error while enqueueing";
+    case H3LIN_E_TIMEOUT: return "device-side wait timed out";
+    case H3LIN_E_UNSUPPORTED: return "device is not sm_103 (GB300)";
+    default: return "unknown status";
+  }
+}
+
+size_t h3lin_codes_bytes(int64_t rows, int64_t K) {
+  if (rows < 1 || K < 64 || K % 64 != 0) return 0;
+  return size_t(rows) * size_t(K / 2);
+}
+
+size_t h3lin_scales_bytes(int64_t rows, int64_t K) {
+  if (rows < 1 || K < 64 || K % 64 != 0) return 0;
+  return size_t((rows + 127) / 128 * 128) * size_t(K / 16);
+}
+
+size_t h3lin_quant_workspace_bytes(void) { return kHeaderBytes; }
+
+size_t h3lin_forward_workspace_bytes(int64_t M, int64_t K, int64_t N, int32_t max_rank) {
+  if (M < 1 || K < 64 || K % 64 != 0 || N < 1 || max_rank < 0) return 0;
+  return forward_layout(M, K, N, max_rank).total;
+}
+
+h3lin_status h3lin_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!ws) return H3LIN_E_INVALID;
+  if (ws_bytes < kHeaderBytes) return H3LIN_E_WORKSPACE;
+  if (cudaMemsetAsync(ws, 0, kHeaderBytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return H3LIN_E_CUDA;
+  }
+  return H3LIN_OK;
+}
+
+h3lin_status h3lin_quantize_act(const void* x, int64_t M, int64_t K, const float* pqs, void* codes, void* scales,
+                                float* tensor_scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return quantize_impl(x, M, K, pqs, codes, scales, tensor_scale, ws, ws_bytes, stream);
+}
+
+h3lin_status h3lin_pack_weight(const void* w, int64_t N, int64_t K, void* codes, void* scales, float* tensor_scale,
+                               void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return quantize_impl(w, N, K, nullptr, codes, scales, tensor_scale, ws, ws_bytes, stream);
+}
+
+h3lin_status h3lin_forward(const void* x, int64_t M, const float* pqs, const h3lin_weight* w, int32_t epilogue,
+                           const h3lin_adapter* adapter, float strength, void* out, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  // ---- validation (nothing is enqueued on error)
+  if (!x || !w || !out || !ws) return H3LIN_E_INVALID;
+  if (!w->codes || !w->scales || !w->tensor_scale) return H3LIN_E_INVALID;
+  if (epilogue != H3LIN_EPI_NONE && epilogue != H3LIN_EPI_SILU_MUL) return H3LIN_E_INVALID;
+  if (!std::isfinite(strength)) return H3LIN_E_INVALID;
+  const int64_t K = w->K, N = w->N;
+  const bool silu = epilogue == H3LIN_EPI_SILU_MUL;
+  if (M < 1 || M > kMaxDim || K < 64 || K > kMaxK || K % 64 != 0 || N < 128 || N > kMaxDim || N % 128 != 0)
+    return H3LIN_E_SHAPE;
+  if (silu && N % 256 != 0) return H3LIN_E_SHAPE;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(ws) || !aligned16(w->codes) || !aligned16(w->scales) ||
+      (pqs && !aligned16(pqs)) || (reinterpret_cast<uintptr_t>(w->tensor_scale) & 3u))
+    return H3LIN_E_ALIGN;
+  const bool lora = adapter != nullptr && strength != 0.0f;
+  int64_t rank = 0;
+  if (lora) {
+    if (!adapter->A || !adapter->B) return H3LIN_E_INVALID;
+    if (!std::isfinite(adapter->alpha)) return H3LIN_E_INVALID;
+    rank = adapter->rank;
+    if (!rank_ok(rank)) return H3LIN_E_SHAPE;
+    if (!aligned16(adapter->A) || !aligned16(adapter->B)) return H3LIN_E_ALIGN;
+  }
+  const ForwardLayout L = forward_layout(M, K, N, rank);
+  if (ws_bytes < L.total) return H3LIN_E_WORKSPACE;
+  DeviceInfo d;
+  h3lin_status s = require_device(&d);
+  if (s != H3LIN_OK) return s;
+
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(wsb + kStatusOffset);
+  float* ts_x = reinterpret_cast<float*>(wsb + kTsOffset);
+  float* partials = reinterpret_cast<float*>(wsb + kPartialsOffset);
+  void* xq = wsb + L.codes;
+  void* xs = wsb + L.scales;
+  void* u = wsb + L.u;
+  void* bp = wsb + L.b;
+
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  // ---- tensor maps
+  if (!make_map(&g.tm_xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, K / 2, M, K / 2, 128, 128)) return H3LIN_E_CUDA;
+  if (!make_map(&g.tm_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, 128)) return H3LIN_E_CUDA;
+  CUtensorMap tm_x, tm_a;
+  int a_box = 0;
+  if (lora) {
+    a_box = rank <= 256 ? int(rank) : int(rank / 2);
+    if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, 128)) return H3LIN_E_CUDA;
+    if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, adapter->A, K, rank, K * 2, 64, a_box))
+      return H3LIN_E_CUDA;
+    if (!make_map(&g.tm_u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, rank, M, rank * 2, 64, 128)) return H3LIN_E_CUDA;
+    if (!make_map(&g.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, bp, rank, N, rank * 2, 64, 128)) return H3LIN_E_CUDA;
+  } else {
+    g.tm_u = g.tm_xq;  // unused by the base-only kernels
+    g.tm_b = g.tm_wq;
+  }
+
+  // ---- kernels
+  const RowPlan plan = plan_rows(M, K, d.sm_count);
+  int nparts = plan.blocks;
+  if (lora) {
+    if (launch_amax_lora(tm_x, tm_a, int(M), int(K), int(rank), a_box, pqs, partials, u, status, d.sm_count,
+                         &nparts, stream) != cudaSuccess)
+      return H3LIN_E_CUDA;
+  } else {
+    if (launch_amax(x, int(M), int(K), pqs, partials, plan, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  }
+  const float lora_k = lora ? strength * (adapter->alpha / float(rank)) : 0.0f;
+  if (launch_quant(x, int(M), int(K), pqs, partials, nparts, xq, xs, ts_x, plan, lora ? adapter->B : nullptr,
+                   lora ? bp : nullptr, lora ? N * rank : 0, lora_k, w->tensor_scale, stream) != cudaSuccess)
+    return H3LIN_E_CUDA;
+  g.xs = static_cast<const uint8_t*>(xs);
+  g.ws = static_cast<const uint8_t*>(w->scales);
+  g.ts_x = ts_x;
+  g.ts_w = w->tensor_scale;
+  g.out = out;
+  g.M = int(M);
+  g.N = int(N);
+  g.K = int(K);
+  g.rank = int(rank);
+  g.ldo = int(silu ? N / 2 : N);
+  g.status = status;
+  g.lora = lora;
+  g.silu = silu;
+  if (launch_fp4gemm(g, d.sm_count, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  return H3LIN_OK;
+}
+
+h3lin_status h3lin_read_status(const void* ws, cudaStream_t stream, int32_t* device_status) {
+  if (!ws || !device_status) return H3LIN_E_INVALID;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return H3LIN_E_CUDA;
+  }
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, static_cast<const uint8_t*>(ws) + kStatusOffset, sizeof(v), cudaMemcpyDeviceToHost) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return H3LIN_E_CUDA;
+  }
+  *device_status = static_cast<int32_t>(v);
+  return H3LIN_OK;
+}
+
+}  // extern "C"

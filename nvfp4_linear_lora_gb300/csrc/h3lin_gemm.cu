@@ -1,0 +1,324 @@
+// The NVFP4 base GEMM with the LoRA up-projection accumulated into the same
+// TMEM tile, and the fused epilogue.
+//
+//   acc[m, n]  = sum_k E2M1(xq) E4M3(sx) * E2M1(wq) E4M3(sw)   (FP4 tensor cores)
+//   acc[m, n] += sum_j u[m, j] * B'[n, j]                        (BF16 tensor cores)
+//   y          = ts_x * ts_w * acc                               (B' carries 1/(ts_x ts_w))
+//   out        = y, or silu(y_gate) * y_up                       (bf16, rows >= M masked)
+//
+// This is `NVFP4_base(x) + strength * (alpha/rank) * B(A(x))` of TURBO.md
+// (h3-blackwell-runtime, "Implementation") with the fused gate/up SiLU*up of
+// the MiniMax-H3 Ultra Fast README ("Active optimization stack", row MLP).
+//
+// Persistent, warp-specialised, one 128 x BN tile per CTA iteration:
+//   warp 0      TMA producer (operand tiles, block-scale atoms by bulk copy)
+//   warp 1      TMEM owner; lane 0 issues tcgen05.cp of the scales and the MMAs
+//   warps 2-9   epilogue: TMEM -> registers, release the accumulator, then
+//               scale / SiLU*up / bf16 / store while the next tile runs
+// Operand stage: A 128 rows x 256 FP4 (128 B rows, 128-byte swizzle), B BN
+// rows, scale atoms 512 B per 128 rows x 64 K.  LoRA stages reuse the ring:
+// u tile 128 x 64 bf16 and B' tile BN x 64 bf16.
+#include "h3lin_device.cuh"
+
+namespace h3lin {
+
+constexpr int kGemmThreads = 320;
+constexpr int kGroupM = 8;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kABytes = 128 * 128;             // 128 rows x 128 B
+  static constexpr int kBBytes = BN * 128;
+  static constexpr int kSfaBytes = 4 * 512;              // 4 atoms (K = 256)
+  static constexpr int kSfbBytes = (BN / 128) * 4 * 512;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kSfCols = 16 + 16 * (BN / 128);   // TMEM columns of one stage's scales
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+  static constexpr int kTmemCols = 512;
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(BN + kStages * kSfCols <= kTmemCols, "TMEM budget");
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = kGroupM * tiles_n;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int gm = min(kGroupM, tiles_m - g * kGroupM);
+  tm = g * kGroupM + r % gm;
+  tn = r / gm;
+}
+
+__device__ __forceinline__ float silu(float g) { return g * __frcp_rn(1.0f + __expf(-g)); }
+
+template <int BN, bool SILU, bool LORA>
+__global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
+    const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_wq,
+    const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_b,
+    const uint8_t* __restrict__ xs, const uint8_t* __restrict__ ws, const float* __restrict__ ts_x,
+    const float* __restrict__ ts_w, __nv_bfloat16* __restrict__ out, int M, int N, int K, int rank, int ldo,
+    uint32_t* __restrict__ status) {
+  using C = GemmCfg<BN>;
+  static_assert(!SILU || BN == 256, "SiLU*up pairs 128 gate and 128 up columns");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tmem_full = empty + C::kStages;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* drain_bar = tmem_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  constexpr int kEpiWarps = 8;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, kEpiWarps);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_xq);
+    tma_prefetch_desc(&tm_wq);
+    if (LORA) {
+      tma_prefetch_desc(&tm_u);
+      tma_prefetch_desc(&tm_b);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, status};
+
+  const int tiles_m = (M + 127) >> 7;
+  const int tiles_n = SILU ? (N / 2) / 128 : N / BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int nk = (K + 255) >> 8;           // FP4 K chunks of 256
+  const int nr = LORA ? (rank + 63) >> 6 : 0;  // LoRA chunks of 64
+  const int k_atoms = K >> 6;              // scale atoms per 128-row block
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t filled = 0, fill_par = 0;
+      int st = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, tiles_m, tiles_n, tm, tn);
+        const int m0 = tm * 128;
+        int brow[2];
+        if (SILU) {
+          brow[0] = tn * 128;
+          brow[1] = N / 2 + tn * 128;
+        } else {
+          brow[0] = tn * BN;
+          brow[1] = tn * BN + 128;
+        }
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
+          const int nsub = min(4, (K - kc * 256) >> 6);
+          uint8_t* base = smem + st * C::kStageBytes;
+          const uint32_t tx = C::kABytes + C::kBBytes + nsub * 512 * (1 + BN / 128);
+          mbar_arrive_expect_tx(&full[st], tx);
+          tma_load_2d(base, &tm_xq, &full[st], kc * 128, m0);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            tma_load_2d(base + C::kABytes + h * 16384, &tm_wq, &full[st], kc * 128, brow[h]);
+          bulk_load(base + C::kABytes + C::kBBytes,
+                    xs + (static_cast<int64_t>(tm) * k_atoms + kc * 4) * 512, nsub * 512, &full[st]);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            bulk_load(base + C::kABytes + C::kBBytes + C::kSfaBytes + h * 2048,
+                      ws + (static_cast<int64_t>(brow[h] >> 7) * k_atoms + kc * 4) * 512, nsub * 512, &full[st]);
+          filled |= 1u << st;
+          fill_par = (fill_par & ~(1u << st)) | (ph << st);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+        for (int rc = 0; rc < nr; ++rc) {
+          if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
+          uint8_t* base = smem + st * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[st], 16384u + BN * 128u);
+          tma_load_2d(base, &tm_u, &full[st], rc * 64, m0);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            tma_load_2d(base + C::kABytes + h * 16384, &tm_b, &full[st], rc * 64, brow[h]);
+          filled |= 1u << st;
+          fill_par = (fill_par & ~(1u << st)) | (ph << st);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+      }
+    producer_done:
+      for (int s = 0; s < C::kStages; ++s)
+        if (filled & (1u << s)) mbar_drain(&full[s], (fill_par >> s) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      const uint32_t idesc_f4 = idesc_nvfp4(BN);
+      const uint32_t idesc_bf = idesc_bf16(BN);
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        if (!mbar_wait(tmem_empty, acc_ph ^ 1, ab)) goto mma_done;
+        tc_fence_after();
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&full[st], ph, ab)) goto mma_done;
+          tc_fence_after();
+          const int nsub = min(4, (K - kc * 256) >> 6);
+          const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
+          const uint32_t b_addr = a_addr + C::kABytes;
+          const uint32_t sfa_addr = b_addr + C::kBBytes;
+          const uint32_t sfb_addr = sfa_addr + C::kSfaBytes;
+          const uint32_t sf_col = tmem + BN + st * C::kSfCols;
+          for (int j = 0; j < nsub; ++j) {
+            tmem_cp_sf_atom(sf_col + 4 * j, sdesc_sf_atom(sfa_addr + j * 512));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tmem_cp_sf_atom(sf_col + 16 + (BN / 128) * 4 * j + 4 * h, sdesc_sf_atom(sfb_addr + h * 2048 + j * 512));
+          }
+          for (int j = 0; j < nsub; ++j) {
+            mma_nvfp4(tmem, sdesc_kmajor_sw128(a_addr + j * 32), sdesc_kmajor_sw128(b_addr + j * 32), idesc_f4,
+                      sf_col + 4 * j, sf_col + 16 + (BN / 128) * 4 * j, (kc | j) != 0);
+          }
+          tc_commit(&empty[st]);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+        for (int rc = 0; rc < nr; ++rc) {
+          if (!mbar_wait(&full[st], ph, ab)) goto mma_done;
+          tc_fence_after();
+          const int nk16 = min(4, (rank - rc * 64) >> 4);
+          const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
+          const uint32_t b_addr = a_addr + C::kABytes;
+          for (int j = 0; j < nk16; ++j)
+            mma_bf16(tmem, sdesc_kmajor_sw128(a_addr + j * 32), sdesc_kmajor_sw128(b_addr + j * 32), idesc_bf, 1u);
+          tc_commit(&empty[st]);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+        tc_commit(tmem_full);
+        acc_ph ^= 1;
+      }
+    mma_done:
+      tc_commit(drain_bar);
+      mbar_drain(drain_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;     // which half of the tile's columns
+    const float scale = __fmul_rn(*ts_x, *ts_w);
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      if (!mbar_wait(tmem_full, acc_ph, ab)) break;
+      tc_fence_after();
+      const int row = tm * 128 + 32 * q + lane;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      constexpr int kChunks = SILU ? 4 : BN / 64;   // x32 column loads per thread
+      uint32_t v[kChunks][32];
+      if (SILU) {
+        tmem_ld32(taddr + half * 64, v[0]);
+        tmem_ld32(taddr + half * 64 + 32, v[1]);
+        tmem_ld32(taddr + 128 + half * 64, v[2]);
+        tmem_ld32(taddr + 128 + half * 64 + 32, v[3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) tmem_ld32(taddr + half * (BN / 2) + 32 * i, v[i]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+      acc_ph ^= 1;
+      if (row < M) {
+        if (SILU) {
+          uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(row) * ldo + tn * 128 + half * 64);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              float hv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float g = __fmul_rn(scale, __uint_as_float(v[i][8 * w + e]));
+                const float u = __fmul_rn(scale, __uint_as_float(v[2 + i][8 * w + e]));
+                hv[e] = __fmul_rn(silu(g), u);
+              }
+              uint4 o;
+              o.x = pack_bf16x2(hv[0], hv[1]);
+              o.y = pack_bf16x2(hv[2], hv[3]);
+              o.z = pack_bf16x2(hv[4], hv[5]);
+              o.w = pack_bf16x2(hv[6], hv[7]);
+              dst[4 * i + w] = o;
+            }
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(row) * ldo + tn * BN + half * (BN / 2));
+#pragma unroll
+          for (int i = 0; i < kChunks; ++i) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint4 o;
+              o.x = pack_bf16x2(__fmul_rn(scale, __uint_as_float(v[i][8 * w + 0])),
+                                __fmul_rn(scale, __uint_as_float(v[i][8 * w + 1])));
+              o.y = pack_bf16x2(__fmul_rn(scale, __uint_as_float(v[i][8 * w + 2])),
+                                __fmul_rn(scale, __uint_as_float(v[i][8 * w + 3])));
+              o.z = pack_bf16x2(__fmul_rn(scale, __uint_as_float(v[i][8 * w + 4])),
+                                __fmul_rn(scale, __uint_as_float(v[i][8 * w + 5])));
+              o.w = pack_bf16x2(__fmul_rn(scale, __uint_as_float(v[i][8 * w + 6])),
+                                __fmul_rn(scale, __uint_as_float(v[i][8 * w + 7])));
+              dst[4 * i + w] = o;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int BN, bool SILU, bool LORA>
+static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t st) {
+  using C = GemmCfg<BN>;
+  auto kern = k_fp4gemm<BN, SILU, LORA>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  const int tiles_m = (a.M + 127) / 128;
+  const int tiles_n = SILU ? (a.N / 2) / 128 : a.N / BN;
+  const int tiles = tiles_m * tiles_n;
+  const int grid = tiles < sm_count ? tiles : sm_count;
+  kern<<<grid, kGemmThreads, C::kSmem, st>>>(a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.xs, a.ws, a.ts_x, a.ts_w,
+                                             static_cast<__nv_bfloat16*>(a.out), a.M, a.N, a.K, a.rank, a.ldo,
+                                             a.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st) {
+  if (a.silu) {
+    return a.lora ? launch_variant<256, true, true>(a, sm_count, st)
+                  : launch_variant<256, true, false>(a, sm_count, st);
+  }
+  if (a.N % 256 == 0) {
+    return a.lora ? launch_variant<256, false, true>(a, sm_count, st)
+                  : launch_variant<256, false, false>(a, sm_count, st);
+  }
+  return a.lora ? launch_variant<128, false, true>(a, sm_count, st)
+                : launch_variant<128, false, false>(a, sm_count, st);
+}
+
+}  // namespace h3lin

@@ -1,0 +1,57 @@
+// Internal declarations shared by the host layer and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/h3lin.h"
+
+namespace h3lin {
+
+// Workspace header: [0] status word (u32), [4] tensor scale of the last
+// quantised activation (f32), [kPartialsOffset ...] per-CTA amax partials.
+constexpr size_t kStatusOffset = 0;
+constexpr size_t kTsOffset = 4;
+constexpr size_t kPartialsOffset = 1024;
+constexpr int kMaxPartials = 4096;
+constexpr size_t kHeaderBytes = kPartialsOffset + kMaxPartials * sizeof(float);  // 17 KB
+constexpr size_t kRegionAlign = 1024;
+
+constexpr int kQuantThreads = 256;
+
+// Launch plans computed on the host.
+struct RowPlan {   // k_amax / k_quant: each thread owns one 16-byte column chunk
+  int blocks;      // grid size
+  int rows_step;   // rows advanced per loop trip (threads per column chunk)
+};
+RowPlan plan_rows(int64_t M, int64_t K, int sm_count);
+
+// Kernel launchers (enqueue only; arguments already validated).
+cudaError_t launch_amax(const void* x, int M, int K, const float* pqs, float* partials, const RowPlan& p,
+                        cudaStream_t st);
+cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
+                         void* codes, void* scales, float* ts_out, const RowPlan& p,
+                         // optional: B' = bf16(B * lora_k / (ts * ts_w)), elems % 8 == 0
+                         const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
+                         cudaStream_t st);
+// amax pass fused with u = A(x) (bf16 [M, rank]); returns grid size in *nparts.
+cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+                             int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
+                             int sm_count, int* nparts, cudaStream_t st);
+// FP4 GEMM + optional LoRA-up + epilogue.
+struct GemmArgs {
+  CUtensorMap tm_xq, tm_wq, tm_u, tm_b;
+  const uint8_t* xs;
+  const uint8_t* ws;
+  const float* ts_x;
+  const float* ts_w;
+  void* out;
+  int M, N, K, rank, ldo;
+  uint32_t* status;
+  bool lora, silu;
+};
+cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st);
+
+}  // namespace h3lin

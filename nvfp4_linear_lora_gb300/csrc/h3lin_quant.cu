@@ -1,0 +1,426 @@
+// Activation side of the dynamic-LoRA NVFP4 linear (TURBO.md,
+// h3-blackwell-runtime, "Implementation"; MiniMax-H3 Ultra Fast README,
+// "Kernel path", item 1: dynamic NVFP4 activation quantisation):
+//
+//   k_amax       amax |x * s| over the tensor -> one partial per CTA
+//   k_amax_lora  the same pass with TMA-staged tiles, fused with the LoRA
+//                down projection u = A(x) on the BF16 tensor cores (tcgen05,
+//                accumulator in TMEM); the LoRA branch sees the original x
+//   k_quant      reduces the partials to the tensor scale, quantises x * s to
+//                E2M1 codes + E4M3 block scales (bit-exact rules below), and
+//                optionally writes B' = B * strength * (alpha/rank) / (ts_x ts_w)
+//                so that the GEMM can accumulate B'(u) into the FP4 tile.
+//
+// Quantisation rules (float32, round to nearest even at every step):
+//   v = x * s;  ts = amax / 2688 (0 -> 1);  per 16 elements:
+//   sb = E4M3_sat(blockamax / (6 ts));  d = E4M3(sb) * ts;  inv = 1 / d;
+//   code = E2M1_sat(v * inv) with the sign of v kept;  inv not finite -> 0.
+#include "h3lin_device.cuh"
+
+namespace h3lin {
+
+// ----------------------------------------------------------------- helpers
+__device__ __forceinline__ void load_scale8(const float* __restrict__ pqs, int c, float (&s)[8]) {
+  if (pqs == nullptr) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = 1.0f;
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(pqs) + 2 * c);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(pqs) + 2 * c + 1);
+    s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+    s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+  }
+}
+
+__device__ __forceinline__ void prescale8(const uint4& w, const float (&s)[8], float (&v)[8]) {
+  v[0] = __fmul_rn(bf16lo(w.x), s[0]);
+  v[1] = __fmul_rn(bf16hi(w.x), s[1]);
+  v[2] = __fmul_rn(bf16lo(w.y), s[2]);
+  v[3] = __fmul_rn(bf16hi(w.y), s[3]);
+  v[4] = __fmul_rn(bf16lo(w.z), s[4]);
+  v[5] = __fmul_rn(bf16hi(w.z), s[5]);
+  v[6] = __fmul_rn(bf16lo(w.w), s[6]);
+  v[7] = __fmul_rn(bf16hi(w.w), s[7]);
+}
+
+__device__ __forceinline__ float absmax8(const float (&v)[8]) {
+  float m = fabsf(v[0]);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+// Block-wide max; every thread gets the result.
+__device__ __forceinline__ float block_max(float m, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  const int nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = red[0];
+  for (int i = 1; i < nw; ++i) m = fmaxf(m, red[i]);
+  return m;
+}
+
+// ----------------------------------------------------------------- k_amax
+// Thread t owns 16-byte column chunk c = t % kc of rows r0, r0 + R, ... with
+// r0 = t / kc (R = rows_step).  The 8 per-channel scales live in registers.
+__global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict__ x, int M, int kc,
+                                                       const float* __restrict__ pqs,
+                                                       float* __restrict__ partials, int rows_step) {
+  __shared__ float red[kQuantThreads / 32];
+  const int tid = blockIdx.x * kQuantThreads + threadIdx.x;
+  const int c = tid % kc;
+  const int r0 = tid / kc;
+  float m = 0.0f;
+  if (r0 < rows_step) {
+    float s[8];
+    load_scale8(pqs, c, s);
+    int row = r0;
+    for (; row + rows_step < M; row += 2 * rows_step) {
+      const uint4 a = x[static_cast<int64_t>(row) * kc + c];
+      const uint4 b = x[static_cast<int64_t>(row + rows_step) * kc + c];
+      float v[8];
+      prescale8(a, s, v);
+      m = fmaxf(m, absmax8(v));
+      prescale8(b, s, v);
+      m = fmaxf(m, absmax8(v));
+    }
+    if (row < M) {
+      float v[8];
+      prescale8(x[static_cast<int64_t>(row) * kc + c], s, v);
+      m = fmaxf(m, absmax8(v));
+    }
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
+// ---------------------------------------------------------------- k_quant
+struct QuantCtx {
+  float ts, six_ts;
+  int M, kc, K;
+  uint32_t* codes;
+  uint8_t* scales;
+};
+
+// Quantise one 8-element chunk (lanes 2j, 2j+1 of an aligned 8-lane group
+// form 16-element block j of the group's 64 columns).
+__device__ __forceinline__ void quant_chunk(const QuantCtx& q, int row, int c, const uint4& w,
+                                            const float (&s)[8], unsigned gmask, int lane) {
+  float v[8];
+  prescale8(w, s, v);
+  float bm = absmax8(v);
+  bm = fmaxf(bm, __shfl_xor_sync(gmask, bm, 1, 8));
+  const uint32_t sb = e4m3_rn_satfinite(__fdiv_rn(bm, q.six_ts));
+  const float d = __fmul_rn(e4m3_to_float(sb), q.ts);
+  const float inv = __frcp_rn(d);
+  float qv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) qv[i] = __fmul_rn(v[i], inv);
+  const uint32_t code = isfinite(inv) ? e2m1x8(qv) : 0u;
+  q.codes[static_cast<int64_t>(row) * q.kc + c] = code;
+  const uint32_t s1 = __shfl_down_sync(gmask, sb, 2, 8);
+  const uint32_t s2 = __shfl_down_sync(gmask, sb, 4, 8);
+  const uint32_t s3 = __shfl_down_sync(gmask, sb, 6, 8);
+  if ((lane & 7) == 0) {
+    *reinterpret_cast<uint32_t*>(q.scales + sf_offset(row, (c >> 1), q.K)) =
+        sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  }
+}
+
+// Rows are visited from the last to the first: the amax pass streamed them
+// in ascending order, so the tail of x is still in L2 when this pass starts.
+__global__ void __launch_bounds__(kQuantThreads) k_quant(
+    const uint4* __restrict__ x, int M, int Mpad, int kc, int K, const float* __restrict__ pqs,
+    const float* __restrict__ partials, int nparts, uint32_t* __restrict__ codes, uint8_t* __restrict__ scales,
+    float* __restrict__ ts_out, int rows_step, const uint4* __restrict__ b_src, uint4* __restrict__ b_dst,
+    int64_t b_chunks, float lora_k, const float* __restrict__ ts_w) {
+  __shared__ float red[kQuantThreads / 32];
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < nparts; i += kQuantThreads) m = fmaxf(m, partials[i]);
+  const float amax = block_max(m, red);
+  float ts = __fdiv_rn(amax, 2688.0f);
+  if (ts == 0.0f) ts = 1.0f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
+  QuantCtx q{ts, __fmul_rn(6.0f, ts), M, kc, K, codes, scales};
+
+  const int tid = blockIdx.x * kQuantThreads + threadIdx.x;
+  const int c = tid % kc;
+  const int r0 = tid / kc;
+  const int lane = threadIdx.x & 31;
+  const unsigned gmask = 0xFFu << (lane & 24);
+  if (r0 < rows_step) {
+    float s[8];
+    load_scale8(pqs, c, s);
+    for (int i = r0; i < Mpad; i += 2 * rows_step) {
+      const int ra = Mpad - 1 - i;
+      const bool has_b = i + rows_step < Mpad;
+      const int rb = Mpad - 1 - (i + rows_step);
+      uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
+      if (ra < M) wa = __ldcs(x + static_cast<int64_t>(ra) * kc + c);
+      if (has_b && rb < M) wb = __ldcs(x + static_cast<int64_t>(rb) * kc + c);
+      if (ra < M) {
+        quant_chunk(q, ra, c, wa, s, gmask, lane);
+      } else if ((lane & 7) == 0) {
+        *reinterpret_cast<uint32_t*>(scales + sf_offset(ra, (c >> 1), K)) = 0u;
+      }
+      if (has_b) {
+        if (rb < M) {
+          quant_chunk(q, rb, c, wb, s, gmask, lane);
+        } else if ((lane & 7) == 0) {
+          *reinterpret_cast<uint32_t*>(scales + sf_offset(rb, (c >> 1), K)) = 0u;
+        }
+      }
+    }
+  }
+  if (b_chunks > 0) {
+    const float cl = __fdiv_rn(lora_k, __fmul_rn(ts, *ts_w));
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * kQuantThreads;
+    for (int64_t i = tid; i < b_chunks; i += nthreads) {
+      const uint4 w = __ldg(b_src + i);
+      uint4 o;
+      o.x = pack_bf16x2(__fmul_rn(bf16lo(w.x), cl), __fmul_rn(bf16hi(w.x), cl));
+      o.y = pack_bf16x2(__fmul_rn(bf16lo(w.y), cl), __fmul_rn(bf16hi(w.y), cl));
+      o.z = pack_bf16x2(__fmul_rn(bf16lo(w.z), cl), __fmul_rn(bf16hi(w.z), cl));
+      o.w = pack_bf16x2(__fmul_rn(bf16lo(w.w), cl), __fmul_rn(bf16hi(w.w), cl));
+      b_dst[i] = o;
+    }
+  }
+}
+
+// ------------------------------------------------------------- k_amax_lora
+// Warp 0: TMA producer.  Warp 1: TMEM owner + MMA issuer.  Warps 2-5: amax of
+// |x * s| read from the staged tile, then the epilogue u = bf16(TMEM).
+// One 128-row tile of x per CTA iteration; K in 64-column stages (x tile
+// 128 x 64 bf16 = 16 KB, A tile rank x 64 bf16), 128-byte swizzle.
+constexpr int kLoraThreads = 192;
+
+__global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
+    const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a, int M, int K,
+    int rank, int a_box_rows, const float* __restrict__ pqs, float* __restrict__ partials,
+    __nv_bfloat16* __restrict__ u, uint32_t* __restrict__ status, int stages, int tmem_cols) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stage_bytes = 16384 + rank * 128;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
+  uint64_t* empty = full + stages;
+  uint64_t* tmem_full = empty + stages;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* drain_bar = tmem_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(abort_flag + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + 4);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 4);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_a);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, status};
+  const int tiles = (M + 127) >> 7;
+  const int nk = K >> 6;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t filled = 0, fill_par = 0;
+      int st = 0;
+      uint32_t ph = 0;
+      const uint32_t tx = 16384u + static_cast<uint32_t>(rank) * 128u;
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
+          uint8_t* base = smem + st * stage_bytes;
+          mbar_arrive_expect_tx(&full[st], tx);
+          tma_load_2d(base, &tm_x, &full[st], kc * 64, t * 128);
+          for (int rb = 0; rb < rank; rb += a_box_rows)
+            tma_load_2d(base + 16384 + rb * 128, &tm_a, &full[st], kc * 64, rb);
+          filled |= 1u << st;
+          fill_par = (fill_par & ~(1u << st)) | (ph << st);
+          if (++st == stages) { st = 0; ph ^= 1; }
+        }
+      }
+    producer_done:
+      for (int s = 0; s < stages; ++s)
+        if (filled & (1u << s)) mbar_drain(&full[s], (fill_par >> s) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      const int n_pieces = rank <= 256 ? 1 : 2;
+      const int piece_n = rank / n_pieces;
+      const uint32_t idesc = idesc_bf16(static_cast<uint32_t>(piece_n));
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        if (!mbar_wait(tmem_empty, acc_ph ^ 1, ab)) goto mma_done;
+        tc_fence_after();
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&full[st], ph, ab)) goto mma_done;
+          tc_fence_after();
+          const uint32_t xa = smem_u32(smem + st * stage_bytes);
+          const uint32_t aa = xa + 16384u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = sdesc_kmajor_sw128(xa + kk * 32);
+            for (int p = 0; p < n_pieces; ++p) {
+              const uint64_t bdesc = sdesc_kmajor_sw128(aa + p * piece_n * 128 + kk * 32);
+              mma_bf16(tmem + p * piece_n, adesc, bdesc, idesc, (kc | kk) != 0);
+            }
+          }
+          tc_commit(&empty[st]);
+          if (++st == stages) { st = 0; ph ^= 1; }
+        }
+        tc_commit(tmem_full);
+        acc_ph ^= 1;
+      }
+    mma_done:
+      tc_commit(drain_bar);
+      mbar_drain(drain_bar, 0);
+    }
+  } else {
+    // amax + epilogue warps; warp w reads TMEM lanes 32 * (w % 4) ...
+    const int q = warp & 3;
+    const int rl = 32 * q + lane;  // row inside the tile
+    float m = 0.0f;
+    int st = 0;
+    uint32_t ph = 0, acc_ph = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      for (int kc = 0; kc < nk; ++kc) {
+        if (!mbar_wait(&full[st], ph, ab)) goto amax_done;
+        const uint8_t* rowp = smem + st * stage_bytes + rl * 128;
+        const float4* sp = pqs ? reinterpret_cast<const float4*>(pqs + kc * 64) : nullptr;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((j ^ (rl & 7)) << 4));
+          float s[8];
+          if (sp) {
+            const float4 a = __ldg(sp + 2 * j), b = __ldg(sp + 2 * j + 1);
+            s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w; s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s[i] = 1.0f;
+          }
+          float v[8];
+          prescale8(w, s, v);
+          m = fmaxf(m, absmax8(v));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (++st == stages) { st = 0; ph ^= 1; }
+      }
+      // epilogue: u[row, :] = bf16(acc)
+      if (!mbar_wait(tmem_full, acc_ph, ab)) goto amax_done;
+      tc_fence_after();
+      {
+        const int row = t * 128 + rl;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        for (int c0 = 0; c0 < rank; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c0, r);
+          tmem_ld_wait();
+          if (row < M) {
+            uint4* dst = reinterpret_cast<uint4*>(u + static_cast<int64_t>(row) * rank + c0);
+            const int nvec = (rank - c0) >= 32 ? 4 : 2;
+            for (int v = 0; v < nvec; ++v) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+              o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+              o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+              o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+              dst[v] = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+      acc_ph ^= 1;
+    }
+  amax_done:
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) red[q] = m;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) partials[blockIdx.x] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// --------------------------------------------------------------- launchers
+RowPlan plan_rows(int64_t M, int64_t K, int sm_count) {
+  const int64_t kc = K / 8;
+  int64_t target = static_cast<int64_t>(sm_count) * 2048;
+  int64_t rows_step = target / kc;
+  if (rows_step < 1) rows_step = 1;
+  const int64_t mpad = ((M + 127) / 128) * 128;
+  if (rows_step > mpad) rows_step = mpad;
+  int64_t blocks = (kc * rows_step + kQuantThreads - 1) / kQuantThreads;
+  while (blocks > kMaxPartials && rows_step > 1) {
+    rows_step /= 2;
+    blocks = (kc * rows_step + kQuantThreads - 1) / kQuantThreads;
+  }
+  return RowPlan{static_cast<int>(blocks), static_cast<int>(rows_step)};
+}
+
+cudaError_t launch_amax(const void* x, int M, int K, const float* pqs, float* partials, const RowPlan& p,
+                        cudaStream_t st) {
+  k_amax<<<p.blocks, kQuantThreads, 0, st>>>(static_cast<const uint4*>(x), M, K / 8, pqs, partials, p.rows_step);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
+                         void* codes, void* scales, float* ts_out, const RowPlan& p, const void* b_src,
+                         void* b_dst, int64_t b_elems, float lora_k, const float* ts_w, cudaStream_t st) {
+  const int Mpad = ((M + 127) / 128) * 128;
+  k_quant<<<p.blocks, kQuantThreads, 0, st>>>(
+      static_cast<const uint4*>(x), M, Mpad, K / 8, K, pqs, partials, nparts, static_cast<uint32_t*>(codes),
+      static_cast<uint8_t*>(scales), ts_out, p.rows_step, static_cast<const uint4*>(b_src),
+      static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+                             int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
+                             int sm_count, int* nparts, cudaStream_t st) {
+  const int stage_bytes = 16384 + rank * 128;
+  constexpr int kSmemLimit = 232448;
+  int stages = (kSmemLimit - 1024 - 256) / stage_bytes;
+  if (stages > 6) stages = 6;
+  if (stages < 2) return cudaErrorInvalidValue;
+  const int smem = stages * stage_bytes + 1024 + 256;
+  int tmem_cols = 32;
+  while (tmem_cols < rank) tmem_cols <<= 1;
+  const int tiles = (M + 127) / 128;
+  int grid = tiles < sm_count ? tiles : sm_count;
+  if (grid > kMaxPartials) grid = kMaxPartials;
+  cudaError_t e = cudaFuncSetAttribute(k_amax_lora, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_amax_lora<<<grid, kLoraThreads, smem, st>>>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, partials,
+                                                static_cast<__nv_bfloat16*>(u), status, stages, tmem_cols);
+  *nparts = grid;
+  return cudaGetLastError();
+}
+
+}  // namespace h3lin

@@ -1,0 +1,231 @@
+"""Thin ctypes binding of ``libh3lin.so`` (C ABI declared in ``include/h3lin.h``).
+
+The ``h3lin_*`` functions mirror the C entry points one to one (plain
+integers for device pointers and streams).  The torch helpers below them only
+marshal arguments: they allocate buffers with torch, pass ``data_ptr()`` and
+the current stream, and raise on a non-zero status.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback — a
+missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libh3lin.so")
+
+H3LIN_OK = 0
+H3LIN_E_INVALID = 1
+H3LIN_E_SHAPE = 2
+H3LIN_E_ALIGN = 3
+H3LIN_E_WORKSPACE = 4
+H3LIN_E_CUDA = 5
+H3LIN_E_TIMEOUT = 6
+H3LIN_E_UNSUPPORTED = 7
+H3LIN_EPI_NONE = 0
+H3LIN_EPI_SILU_MUL = 1
+
+
+class H3linError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({h3lin_status_string(status)})")
+
+
+class h3lin_weight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class h3lin_adapter(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("rank", ctypes.c_int32),
+                ("alpha", ctypes.c_float)]
+
+
+_lib = None
+_vp, _i64, _i32, _sz, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+
+_SIGNATURES = {
+    "h3lin_abi_version": (_i32, []),
+    "h3lin_status_string": (ctypes.c_char_p, [_i32]),
+    "h3lin_codes_bytes": (_sz, [_i64, _i64]),
+    "h3lin_scales_bytes": (_sz, [_i64, _i64]),
+    "h3lin_quant_workspace_bytes": (_sz, []),
+    "h3lin_forward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
+    "h3lin_workspace_init": (_i32, [_vp, _sz, _vp]),
+    "h3lin_quantize_act": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "h3lin_pack_weight": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "h3lin_forward": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), _i32, ctypes.POINTER(h3lin_adapter),
+                             _f32, _vp, _vp, _sz, _vp]),
+    "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+}
+
+
+def lib():
+    """Load ``libh3lin.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with nvfp4_linear_lora_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------- C entry points
+def h3lin_abi_version():
+    return lib().h3lin_abi_version()
+
+
+def h3lin_status_string(status):
+    return lib().h3lin_status_string(int(status)).decode()
+
+
+def h3lin_codes_bytes(rows, K):
+    return lib().h3lin_codes_bytes(rows, K)
+
+
+def h3lin_scales_bytes(rows, K):
+    return lib().h3lin_scales_bytes(rows, K)
+
+
+def h3lin_quant_workspace_bytes():
+    return lib().h3lin_quant_workspace_bytes()
+
+
+def h3lin_forward_workspace_bytes(M, K, N, max_rank):
+    return lib().h3lin_forward_workspace_bytes(M, K, N, max_rank)
+
+
+def h3lin_workspace_init(ws, ws_bytes, stream):
+    return lib().h3lin_workspace_init(ws, ws_bytes, stream)
+
+
+def h3lin_quantize_act(x, M, K, pqs, codes, scales, tensor_scale, ws, ws_bytes, stream):
+    return lib().h3lin_quantize_act(x, M, K, pqs, codes, scales, tensor_scale, ws, ws_bytes, stream)
+
+
+def h3lin_pack_weight(w, N, K, codes, scales, tensor_scale, ws, ws_bytes, stream):
+    return lib().h3lin_pack_weight(w, N, K, codes, scales, tensor_scale, ws, ws_bytes, stream)
+
+
+def h3lin_forward(x, M, pqs, weight, epilogue, adapter, strength, out, ws, ws_bytes, stream):
+    wp = ctypes.byref(weight) if weight is not None else None
+    ap = ctypes.byref(adapter) if adapter is not None else None
+    return lib().h3lin_forward(x, M, pqs, wp, epilogue, ap, strength, out, ws, ws_bytes, stream)
+
+
+def h3lin_read_status(ws, stream):
+    v = _i32(-1)
+    st = lib().h3lin_read_status(ws, stream, ctypes.byref(v))
+    return st, v.value
+
+
+# ------------------------------------------------------- torch marshalling
+def _torch():
+    import torch
+    return torch
+
+
+def _stream():
+    return _torch().cuda.current_stream().cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(status, where):
+    if status != H3LIN_OK:
+        raise H3linError(status, where)
+
+
+@dataclass
+class PackedWeight:
+    """NVFP4 weight owned by torch tensors: codes u8 [N, K/2], native scales,
+    fp32 tensor scale (device)."""
+    codes: object
+    scales: object
+    tensor_scale: object
+    N: int
+    K: int
+
+    def c_struct(self):
+        return h3lin_weight(self.codes.data_ptr(), self.scales.data_ptr(), self.tensor_scale.data_ptr(),
+                            self.N, self.K)
+
+
+@dataclass
+class Adapter:
+    """A resident LoRA adapter: A bf16 [rank, K], B bf16 [N, rank] on the device."""
+    A: object
+    B: object
+    rank: int
+    alpha: float
+
+    def c_struct(self):
+        return h3lin_adapter(self.A.data_ptr(), self.B.data_ptr(), self.rank, self.alpha)
+
+
+def new_workspace(nbytes, device="cuda"):
+    torch = _torch()
+    ws = torch.empty(int(nbytes), dtype=torch.uint8, device=device)
+    _check(h3lin_workspace_init(ws.data_ptr(), ws.numel(), _stream()), "h3lin_workspace_init")
+    return ws
+
+
+def quantize_act(x, pre_quant_scale=None, workspace=None):
+    """x bf16 [M, K] (cuda) -> (codes u8 [M, K/2], native scales u8, tensor scale f32 [1])."""
+    torch = _torch()
+    M, K = x.shape
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(h3lin_scales_bytes(M, K), dtype=torch.uint8, device=x.device)
+    ts = torch.empty(1, dtype=torch.float32, device=x.device)
+    ws = workspace if workspace is not None else new_workspace(h3lin_quant_workspace_bytes(), x.device)
+    _check(h3lin_quantize_act(x.data_ptr(), M, K, _ptr(pre_quant_scale), codes.data_ptr(), scales.data_ptr(),
+                              ts.data_ptr(), ws.data_ptr(), ws.numel(), _stream()), "h3lin_quantize_act")
+    return codes, scales, ts
+
+
+def pack_weight(w, workspace=None):
+    """w bf16 [N, K] (cuda) -> PackedWeight."""
+    torch = _torch()
+    N, K = w.shape
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty(h3lin_scales_bytes(N, K), dtype=torch.uint8, device=w.device)
+    ts = torch.empty(1, dtype=torch.float32, device=w.device)
+    ws = workspace if workspace is not None else new_workspace(h3lin_quant_workspace_bytes(), w.device)
+    _check(h3lin_pack_weight(w.data_ptr(), N, K, codes.data_ptr(), scales.data_ptr(), ts.data_ptr(),
+                             ws.data_ptr(), ws.numel(), _stream()), "h3lin_pack_weight")
+    return PackedWeight(codes, scales, ts, N, K)
+
+
+def forward(x, weight, pre_quant_scale=None, adapter=None, strength=1.0, silu_mul=False, out=None,
+            workspace=None):
+    """One projection through ``h3lin_forward``; returns ``out`` (bf16)."""
+    torch = _torch()
+    M = x.shape[0]
+    n_out = weight.N // 2 if silu_mul else weight.N
+    if out is None:
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = new_workspace(h3lin_forward_workspace_bytes(M, weight.K, weight.N,
+                                                                adapter.rank if adapter else 0), x.device)
+    wc = weight.c_struct()
+    ac = adapter.c_struct() if adapter is not None else None
+    _check(h3lin_forward(x.data_ptr(), M, _ptr(pre_quant_scale), wc,
+                         H3LIN_EPI_SILU_MUL if silu_mul else H3LIN_EPI_NONE, ac, float(strength),
+                         out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream()), "h3lin_forward")
+    return out
+
+
+def read_status(workspace):
+    st, v = h3lin_read_status(workspace.data_ptr(), _stream())
+    _check(st, "h3lin_read_status")
+    return v

@@ -1,0 +1,138 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point declared in include/h3lin.h, sizes are right, and invalid
+arguments are rejected on the host before anything is enqueued."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from nvfp4_linear_lora_gb300 import build as h3build
+from nvfp4_linear_lora_gb300 import h3lin
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    h3build.build()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "h3lin.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(h3lin_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ["h3lin_pack_weight", "h3lin_quantize_act", "h3lin_forward", "h3lin_read_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = h3lin.lib()
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_abi_version_and_strings():
+    assert h3lin.h3lin_abi_version() == 1
+    for s in range(8):
+        assert len(h3lin.h3lin_status_string(s)) > 0
+
+
+def test_sizes():
+    assert h3lin.h3lin_codes_bytes(200, 256) == 200 * 128
+    assert h3lin.h3lin_scales_bytes(200, 256) == 256 * 16
+    assert h3lin.h3lin_scales_bytes(37726, 5120) == 37760 * 320
+    assert h3lin.h3lin_codes_bytes(10, 100) == 0 and h3lin.h3lin_scales_bytes(0, 64) == 0
+    ws = h3lin.h3lin_forward_workspace_bytes(9437, 5120, 15360, 384)
+    need = 9437 * 2560 + 9472 * 320 + 9437 * 384 * 2 + 15360 * 384 * 2
+    assert need < ws < need + 64 * 1024
+    assert h3lin.h3lin_forward_workspace_bytes(9437, 5120, 15360, 0) < ws
+
+
+A = 0x10000  # an aligned fake device address (never dereferenced on error paths)
+
+
+def _weight(N=384, K=256):
+    return h3lin.h3lin_weight(A, A, A, N, K)
+
+
+def _fwd(**kw):
+    args = dict(x=A, M=200, pqs=None, weight=_weight(), epilogue=0, adapter=None, strength=1.0, out=A, ws=A,
+                ws_bytes=1 << 30, stream=None)
+    args.update(kw)
+    return h3lin.h3lin_forward(args["x"], args["M"], args["pqs"], args["weight"], args["epilogue"],
+                               args["adapter"], args["strength"], args["out"], args["ws"], args["ws_bytes"],
+                               args["stream"])
+
+
+def test_forward_rejects_invalid_arguments():
+    E = h3lin
+    assert _fwd(x=None) == E.H3LIN_E_INVALID
+    assert _fwd(out=None) == E.H3LIN_E_INVALID
+    assert _fwd(weight=h3lin.h3lin_weight(None, A, A, 384, 256)) == E.H3LIN_E_INVALID
+    assert _fwd(epilogue=7) == E.H3LIN_E_INVALID
+    assert _fwd(strength=math.nan) == E.H3LIN_E_INVALID
+    assert _fwd(strength=math.inf) == E.H3LIN_E_INVALID
+    assert _fwd(M=0) == E.H3LIN_E_SHAPE
+    assert _fwd(weight=_weight(384, 200)) == E.H3LIN_E_SHAPE          # K % 64
+    assert _fwd(weight=_weight(300, 256)) == E.H3LIN_E_SHAPE          # N % 128
+    assert _fwd(weight=_weight(384, 256), epilogue=1) == E.H3LIN_E_SHAPE  # SiLU needs N % 256
+    assert _fwd(x=A + 8) == E.H3LIN_E_ALIGN
+    assert _fwd(out=A + 2) == E.H3LIN_E_ALIGN
+    assert _fwd(pqs=A + 4) == E.H3LIN_E_ALIGN
+    assert _fwd(ws_bytes=1024) == E.H3LIN_E_WORKSPACE
+
+
+@pytest.mark.parametrize("rank,ok", [(16, True), (24, False), (128, True), (256, True), (272, False),
+                                     (288, True), (384, True), (512, True), (544, False), (8, False), (0, False)])
+def test_forward_rank_rule(rank, ok):
+    ad = h3lin.h3lin_adapter(A, A, rank, float(rank))
+    st = _fwd(adapter=ad)
+    if ok:
+        assert st not in (h3lin.H3LIN_E_SHAPE, h3lin.H3LIN_E_INVALID), st
+    else:
+        assert st == h3lin.H3LIN_E_SHAPE
+
+
+def test_forward_adapter_checks():
+    E = h3lin
+    assert _fwd(adapter=h3lin.h3lin_adapter(None, A, 16, 16.0)) == E.H3LIN_E_INVALID
+    assert _fwd(adapter=h3lin.h3lin_adapter(A, A, 16, math.nan)) == E.H3LIN_E_INVALID
+    assert _fwd(adapter=h3lin.h3lin_adapter(A + 4, A, 16, 16.0)) == E.H3LIN_E_ALIGN
+    # strength 0 selects the base path: the adapter is not even looked at
+    bad = h3lin.h3lin_adapter(None, None, 3, math.nan)
+    assert _fwd(adapter=bad, strength=0.0) not in (E.H3LIN_E_INVALID, E.H3LIN_E_SHAPE)
+
+
+def test_quantize_rejects_invalid_arguments():
+    E = h3lin
+    q = lambda **kw: h3lin.h3lin_quantize_act(kw.get("x", A), kw.get("M", 10), kw.get("K", 64), kw.get("pqs"),
+                                              kw.get("codes", A), kw.get("scales", A), kw.get("ts", A),
+                                              kw.get("ws", A), kw.get("ws_bytes", 1 << 20), None)
+    assert q(x=None) == E.H3LIN_E_INVALID
+    assert q(ts=None) == E.H3LIN_E_INVALID
+    assert q(K=96) == E.H3LIN_E_SHAPE
+    assert q(M=0) == E.H3LIN_E_SHAPE
+    assert q(codes=A + 1) == E.H3LIN_E_ALIGN
+    assert q(ws_bytes=16) == E.H3LIN_E_WORKSPACE
+    assert h3lin.h3lin_pack_weight(A, 0, 64, A, A, A, A, 1 << 20, None) == E.H3LIN_E_SHAPE
+
+
+@pytest.mark.skipif(__import__("tests._util", fromlist=["have_gpu"]).have_gpu(), reason="GPU present")
+def test_valid_call_without_gpu_reports_cuda_error():
+    # every host check passes; the call then fails to find a device and says so
+    assert _fwd() in (h3lin.H3LIN_E_CUDA, h3lin.H3LIN_E_UNSUPPORTED)
+
+
+def test_native_scale_layout_is_a_bijection():
+    from tests._util import native_scale_offsets
+    for rows, K in [(128, 64), (200, 256), (300, 320)]:
+        off = native_scale_offsets(rows, K).reshape(-1)
+        assert len(set(off.tolist())) == off.size
+        assert off.max() < h3lin.h3lin_scales_bytes(rows, K)

@@ -1,0 +1,145 @@
+"""GPU parity of h3lin_forward against the oracle at sizes the oracle finishes
+in seconds: several tiles, ragged M tails, every epilogue/adapter mode, plus
+the method's exactness and switching properties."""
+import numpy as np
+import pytest
+
+from tests._util import assert_parity, have_gpu
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not have_gpu(), reason="needs a CUDA GPU")]
+
+torch = pytest.importorskip("torch")
+
+from nvfp4_linear_lora_gb300 import build as h3build  # noqa: E402
+from nvfp4_linear_lora_gb300 import configs, h3lin, synth  # noqa: E402
+from oracle import linear  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    h3build.build()
+
+
+def to_dev(p):
+    d = {"x": synth.to_bf16_tensor(p["x"]).cuda(),
+         "pqs": torch.from_numpy(p["pqs"]).cuda() if p["pqs"] is not None else None,
+         "W": synth.to_bf16_tensor(p["W"]).cuda()}
+    ad = p["adapter"]
+    d["adapter"] = None if ad is None else h3lin.Adapter(synth.to_bf16_tensor(ad["A"]).cuda(),
+                                                         synth.to_bf16_tensor(ad["B"]).cuda(), ad["rank"], ad["alpha"])
+    return d
+
+
+def run(p, strength=1.0, silu=False, use_adapter=True, dev=None, pw=None):
+    dev = dev or to_dev(p)
+    pw = pw or h3lin.pack_weight(dev["W"])
+    out = h3lin.forward(dev["x"], pw, dev["pqs"], dev["adapter"] if use_adapter else None, strength, silu)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), dev, pw
+
+
+def ref(p, strength=1.0, silu=False, use_adapter=True):
+    return linear.forward(p["x"], linear.pack_weight(p["W"]), p["pqs"], p["adapter"] if use_adapter else None,
+                          strength, silu)
+
+
+CASES = [
+    # M, K, N, rank, silu
+    (200, 256, 384, 16, False),      # the tiny single-projection workload
+    (1, 64, 128, 16, False),
+    (129, 320, 256, 32, False),
+    (300, 256, 512, 64, True),
+    (130, 128, 256, 128, True),
+    (257, 512, 384, 384, False),
+    (64, 1024, 768, 256, False),
+    (384, 256, 256, 288, False),
+    (1000, 1024, 1280, 128, False),
+]
+
+
+@pytest.mark.parametrize("M,K,N,rank,silu", CASES)
+def test_forward_matches_oracle(M, K, N, rank, silu):
+    p = synth.projection(1000 + M + K + N + rank, M, K, N, rank, outlier_frac=0.01)
+    got, _, _ = run(p, silu=silu)
+    assert got.shape == (M, N // 2 if silu else N)
+    assert_parity(got, ref(p, silu=silu), f"M={M} K={K} N={N} r={rank} silu={silu}")
+
+
+@pytest.mark.parametrize("M,K,N,rank,silu", CASES[:6])
+def test_base_path_matches_oracle(M, K, N, rank, silu):
+    p = synth.projection(2000 + M, M, K, N, rank)
+    got, _, _ = run(p, silu=silu, use_adapter=False)
+    assert_parity(got, ref(p, silu=silu, use_adapter=False), "base")
+
+
+def test_tiny_workload_matches_oracle():
+    c = configs.TINY
+    p = synth.projection(c["seed"], c["M"], c["K"], c["N"], c["rank"])
+    got, _, _ = run(p)
+    assert_parity(got, ref(p), "tiny")
+
+
+@pytest.mark.parametrize("silu", [False, True])
+def test_disabled_exactness_bitwise(silu):
+    p = synth.projection(7, 333, 256, 512, 128)
+    base, dev, pw = run(p, use_adapter=False, silu=silu)
+    zero, _, _ = run(p, strength=0.0, silu=silu, dev=dev, pw=pw)
+    assert np.array_equal(base.view(np.uint32), zero.view(np.uint32))
+    one, _, _ = run(p, strength=1.0, silu=silu, dev=dev, pw=pw)
+    assert not np.array_equal(base, one)
+
+
+def test_adapter_switching_per_call():
+    M, K, N = 300, 256, 384
+    p = synth.projection(11, M, K, N, 128)
+    rng = np.random.default_rng(12)
+    ad2 = synth.adapter(rng, N, K, 384)
+    dev = to_dev(p)
+    pw = h3lin.pack_weight(dev["W"])
+    a1 = dev["adapter"]
+    a2 = h3lin.Adapter(synth.to_bf16_tensor(ad2["A"]).cuda(), synth.to_bf16_tensor(ad2["B"]).cuda(), 384, 384.0)
+    wref = linear.pack_weight(p["W"])
+    outs = []
+    for ad, s in [(a1, 1.0), (a2, 0.5), (None, 1.0), (a1, 1.0), (a2, 1.0)]:
+        o = h3lin.forward(dev["x"], pw, dev["pqs"], ad, s)
+        outs.append(o.float().cpu().numpy())
+    for o, (ad, s) in zip(outs, [(p["adapter"], 1.0), (ad2, 0.5), (None, 1.0), (p["adapter"], 1.0), (ad2, 1.0)]):
+        assert_parity(o, linear.forward(p["x"], wref, p["pqs"], ad, s), "switch")
+    assert np.array_equal(outs[0], outs[3])        # no state carried between calls
+
+
+def test_strength_linearity():
+    p = synth.projection(21, 256, 256, 256, 64)
+    y0, dev, pw = run(p, strength=0.0)
+    yh, _, _ = run(p, strength=0.5, dev=dev, pw=pw)
+    y1, _, _ = run(p, strength=1.0, dev=dev, pw=pw)
+    assert_parity(yh, ref(p, 0.5), "s=0.5")
+    d1, dh = y1 - y0, yh - y0
+    assert np.linalg.norm(d1 - 2 * dh) / np.linalg.norm(d1) < 2e-2
+
+
+def test_zero_base_weight_is_pure_lora():
+    p = synth.projection(31, 200, 256, 384, 32)
+    p["W"] = np.zeros_like(p["W"])
+    got, _, _ = run(p)
+    assert_parity(got, ref(p), "pure LoRA")
+
+
+def test_rows_beyond_M_untouched():
+    p = synth.projection(41, 150, 256, 256, 16)
+    dev = to_dev(p)
+    pw = h3lin.pack_weight(dev["W"])
+    big = torch.full((256, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    h3lin.forward(dev["x"], pw, dev["pqs"], dev["adapter"], 1.0, False, out=big[:150])
+    torch.cuda.synchronize()
+    assert torch.all(big[150:] == 7.0)
+    assert_parity(big[:150].float().cpu().numpy(), ref(p), "canary")
+
+
+def test_device_status_clean():
+    p = synth.projection(51, 100, 128, 128, 16)
+    dev = to_dev(p)
+    pw = h3lin.pack_weight(dev["W"])
+    ws = h3lin.new_workspace(h3lin.h3lin_forward_workspace_bytes(100, 128, 128, 16))
+    h3lin.forward(dev["x"], pw, dev["pqs"], dev["adapter"], 1.0, False, workspace=ws)
+    assert h3lin.read_status(ws) == 0
