@@ -1,0 +1,423 @@
+"""Benchmark of the DiT block's projection hot path on GB300.
+
+One step = the four dynamic-LoRA NVFP4 projections of one transformer block
+at packed sequence length S = 37726 (fused QKV 5120->15360 rank 384,
+attention-out 5120->5120, fused gate/up 5120->27648 with SiLU*up, down
+13824->5120, ranks 128, alpha = rank, strength 1), run back to back on one
+stream through the C ABI; down consumes gate/up's output.  Inputs are seeded
+synthetic tensors already resident in HBM (each activation is larger than L2,
+so no flush is needed between steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded row x column sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_linear_lora_gb300 import configs, synth  # noqa: E402
+
+METRIC = "NVFP4+LoRA projection TFLOP/s at S=37726 (% of dense FP4 peak); ms/block"
+FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor ratio on GB300
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--S", type=int, default=configs.BLOCK_S)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU-oracle sample time")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def block_flops(S):
+    """(total, base FP4, LoRA down, LoRA up) algorithmic FLOPs of one block."""
+    base = down = up = 0
+    for _, K, N, r, _ in configs.BLOCK_PROJECTIONS:
+        base += 2 * S * K * N
+        down += 2 * S * K * r
+        up += 2 * S * r * N
+    return base + down + up, base, down, up
+
+
+# ----------------------------------------------------------------- workload
+def make_block_inputs(S, seed=configs.BLOCK_SEED):
+    """Host inputs of the block, one generator in block order: per projection
+    x (not for down, which consumes gate/up's output), s, W, A, B."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for name, K, N, r, silu in configs.BLOCK_PROJECTIONS:
+        x = synth.activation(rng, S, K) if name != "down" else None
+        s = synth.pre_quant_scale(rng, K)
+        W = synth.weight(rng, N, K)
+        ad = synth.adapter(rng, N, K, r)
+        out.append(dict(name=name, K=K, N=N, rank=r, silu=silu, x=x, pqs=s, W=W, adapter=ad))
+    return out
+
+
+class Block:
+    """Device-resident block: packed weights, adapters, workspaces, outputs."""
+
+    def __init__(self, host, S, device):
+        import torch
+
+        from nvfp4_linear_lora_gb300 import h3lin
+        self.h3lin = h3lin
+        self.S = S
+        self.proj = []
+        stream = torch.cuda.current_stream().cuda_stream
+        for p in host:
+            d = dict(p)
+            d["x_dev"] = synth.to_bf16_tensor(p["x"]).to(device) if p["x"] is not None else None
+            d["pqs_dev"] = torch.from_numpy(p["pqs"]).to(device)
+            Wd = synth.to_bf16_tensor(p["W"]).to(device)
+            d["pw"] = h3lin.pack_weight(Wd)
+            del Wd
+            a = p["adapter"]
+            d["ad"] = h3lin.Adapter(synth.to_bf16_tensor(a["A"]).to(device), synth.to_bf16_tensor(a["B"]).to(device),
+                                    a["rank"], a["alpha"])
+            n_out = p["N"] // 2 if p["silu"] else p["N"]
+            d["out"] = torch.empty((S, n_out), dtype=torch.bfloat16, device=device)
+            wsb = h3lin.h3lin_forward_workspace_bytes(S, p["K"], p["N"], p["rank"])
+            d["ws"] = h3lin.new_workspace(wsb, device)
+            d["wc"] = d["pw"].c_struct()
+            d["ac"] = d["ad"].c_struct()
+            d["stream"] = stream
+            self.proj.append(d)
+        # down consumes gate/up's output
+        self.proj[3]["x_dev"] = self.proj[2]["out"]
+        torch.cuda.synchronize()
+
+    def launches_per_step(self):
+        return 3 * len(self.proj)
+
+    def step(self, gemm_events=None):
+        """One block.  With ``gemm_events`` (list of (start, stop) per
+        projection) the two stages are enqueued separately with events around
+        the GEMM kernel, on the same stream."""
+        h = self.h3lin
+        for i, d in enumerate(self.proj):
+            if gemm_events is None:
+                st = h.h3lin_forward(d["x_dev"].data_ptr(), self.S, d["pqs_dev"].data_ptr(), d["wc"],
+                                     h.H3LIN_EPI_SILU_MUL if d["silu"] else h.H3LIN_EPI_NONE, d["ac"], 1.0,
+                                     d["out"].data_ptr(), h.H3LIN_OUT_BF16, d["ws"].data_ptr(), d["ws"].numel(),
+                                     d["stream"])
+                if st:
+                    raise h.H3linError(st, "h3lin_forward")
+            else:
+                st = h.h3lin_forward_prepare(d["x_dev"].data_ptr(), self.S, d["pqs_dev"].data_ptr(), d["wc"], d["ac"],
+                                             1.0, d["ws"].data_ptr(), d["ws"].numel(), d["stream"])
+                if st:
+                    raise h.H3linError(st, "h3lin_forward_prepare")
+                gemm_events[i][0].record()
+                st = h.h3lin_forward_gemm(self.S, d["wc"], h.H3LIN_EPI_SILU_MUL if d["silu"] else h.H3LIN_EPI_NONE,
+                                          d["ac"], 1.0, d["out"].data_ptr(), h.H3LIN_OUT_BF16, d["ws"].data_ptr(),
+                                          d["ws"].numel(), d["stream"])
+                if st:
+                    raise h.H3linError(st, "h3lin_forward_gemm")
+                gemm_events[i][1].record()
+
+    def check_status(self):
+        for d in self.proj:
+            v = self.h3lin.read_status(d["ws"])
+            if v != 0:
+                raise RuntimeError(f"device status {v} in projection {d['name']}")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [t.strip() for t in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample_run(host, m_rows, n_cols, seed=123, packed=None):
+    """Run the oracle on a row x output-column sample of every projection as
+    its own call (amax over the sampled rows).  With only a column sample of
+    gate/up there is no full SiLU*up row to feed down, so down's sampled rows
+    are drawn from N(0, 1) instead.  Returns (seconds, flops)."""
+    from oracle import linear
+    rng = np.random.default_rng(seed)
+    t_total, flops = 0.0, 0
+    for i, p in enumerate(host):
+        K, N, r, silu = p["K"], p["N"], p["rank"], p["silu"]
+        wq, ws, tsw = packed[i] if packed else linear.pack_weight(p["W"])
+        if silu:
+            half = N // 2
+            nc = min(n_cols // 2, half)
+            c = np.sort(rng.choice(half, nc, replace=False))
+            cols = np.concatenate([c, c + half])
+        else:
+            nc = min(n_cols, N)
+            cols = np.sort(rng.choice(N, nc, replace=False))
+        weight = (wq[cols], ws[cols], tsw)
+        ad = dict(p["adapter"])
+        ad["B"] = ad["B"][cols]
+        if p["x"] is not None:
+            rows = np.sort(rng.choice(p["x"].shape[0], m_rows, replace=False))
+            x = p["x"][rows]
+        else:
+            x = synth.bf16_round(rng.standard_normal((m_rows, K)).astype(np.float32))
+        t0 = time.perf_counter()
+        y = linear.forward(x, weight, p["pqs"], ad, 1.0, silu)
+        t_total += time.perf_counter() - t0
+        flops += 2 * x.shape[0] * (K * len(cols) + K * r + r * len(cols))
+    return t_total, flops
+
+
+def pack_all(host):
+    from oracle import linear
+    return [linear.pack_weight(p["W"]) for p in host]
+
+
+def calibrate_sample(host, packed, seconds):
+    """Pick (rows, cols) so that one oracle sample run takes about ``seconds``."""
+    m, n = 16, 256
+    t, _ = oracle_sample_run(host, m, n, packed=packed)
+    scale = max(0.25, min(64.0, seconds / max(t, 1e-3)))
+    n = int(max(128, min(8192, n * scale)) // 128 * 128)
+    return m, n
+
+
+def cpu_info():
+    return os.cpu_count() or 1
+
+
+# -------------------------------------------------------------------- arms
+def reference_arm(a, rank, world):
+    if rank != 0:
+        return 0
+    S = a.S
+    host = make_block_inputs(S)
+    packed = pack_all(host)
+    per_step = 150.0 / max(1, a.steps + a.warmup)
+    m, n = calibrate_sample(host, packed, per_step)
+    for _ in range(a.warmup):
+        oracle_sample_run(host, m, n, packed=packed)
+    t_sum, f_sum = 0.0, 0
+    for k in range(a.steps):
+        t, f = oracle_sample_run(host, m, n, seed=1000 + k, packed=packed)
+        t_sum += t
+        f_sum += f
+    value = f_sum / t_sum / 1e12
+    sample = f"{m} rows x {n} output columns of each of the 4 projections per step (S={S} workload)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * t_sum / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"dit_block_4proj_S{S}", "S": S, "hidden": configs.HIDDEN, "mlp": configs.MLP,
+                       "ranks": [p[3] for p in configs.BLOCK_PROJECTIONS], "strength": 1.0},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_info(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def native_arm(a, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from nvfp4_linear_lora_gb300 import build as h3build
+    h3build.build()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    S = a.S
+    host = make_block_inputs(S)
+    blk = Block(host, S, device)
+    peaks, peak_kind = load_peaks()
+    total, base, ldown, lup = block_flops(S)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # warm-up
+    for _ in range(a.warmup):
+        blk.step()
+    torch.cuda.synchronize()
+    blk.check_status()
+
+    # timed region: K steps, GEMM kernels bracketed by events on the launching stream
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in blk.proj]
+          for _ in range(a.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local_rank) if rank == 0 else None
+    time.sleep(0.3 if clk else 0)
+    t0.record()
+    for k in range(a.steps):
+        blk.step(gemm_events=ev[k])
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = clk.stop() if clk else None
+    barrier()
+    ms = t0.elapsed_time(t1) / a.steps
+    gemm_ms = [statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(a.steps))
+               for i in range(len(blk.proj))]
+    blk.check_status()
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * total / (ms * 1e-3) / 1e12
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not a.no_e2e:
+        xs_host = [synth.to_bf16_tensor(p["x"]).pin_memory() for p in host if p["x"] is not None]
+        x_dev = [d["x_dev"] for d in blk.proj if d["x"] is not None]
+        outs = [blk.proj[0]["out"], blk.proj[1]["out"], blk.proj[3]["out"]]
+        outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in xs_host)
+        d2h = sum(t.numel() * t.element_size() for t in outs_host)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(a.e2e_steps):
+            for hsrc, ddst in zip(xs_host, x_dev):
+                ddst.copy_(hsrc, non_blocking=True)
+            blk.step()
+            for dsrc, hdst in zip(outs, outs_host):
+                hdst.copy_(dsrc, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1) / a.e2e_steps
+        if world > 1:
+            t = torch.tensor([ems], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * total / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return 0
+
+    # roofline of the dominant kernel (the FP4 GEMM with LoRA-up), live event timing
+    gemm_total_ms = sum(gemm_ms)
+    gemm_fp4 = base
+    gemm_bf16 = lup
+    peak_bf16 = peaks["bf16_tflops_sustained"]
+    peak_fp4 = peak_bf16 * FP4_OVER_BF16
+    ideal_s = gemm_fp4 / (peak_fp4 * 1e12) + gemm_bf16 / (peak_bf16 * 1e12)
+    mixed_peak = (gemm_fp4 + gemm_bf16) / ideal_s / 1e12
+    achieved = (gemm_fp4 + gemm_bf16) / (gemm_total_ms * 1e-3) / 1e12
+    roofline = {"kernel": "k_fp4gemm", "bound": "tensor", "achieved": achieved, "peak": mixed_peak,
+                "unit": "TFLOP/s", "frac": achieved / mixed_peak, "traffic": None,
+                "peak_basis": f"{peak_kind} sustained bf16 {peak_bf16:.1f} TF/s x {FP4_OVER_BF16:g} for the FP4 "
+                              f"part, x 1 for the BF16 LoRA-up part, time-weighted over this kernel's FLOP mix",
+                "gemm_ms_per_projection": dict(zip([d["name"] for d in blk.proj], gemm_ms))}
+
+    cpu = None
+    if not a.no_cpu_baseline and world == 1:
+        packed = pack_all(host)
+        m, n = calibrate_sample(host, packed, a.cpu_seconds)
+        t, f = oracle_sample_run(host, m, n, seed=7, packed=packed)
+        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cpu_info(), "kind": "oracle",
+               "sample": f"{m} rows x {n} output columns of each projection (same S={S} workload), {t:.1f} s"}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e2m1+bf16", "data": "synthetic",
+            "config": {"workload": f"dit_block_4proj_S{S}", "S": S, "hidden": configs.HIDDEN, "mlp": configs.MLP,
+                       "ranks": [p[3] for p in configs.BLOCK_PROJECTIONS], "strength": 1.0,
+                       "l2": "inputs larger than L2 (each activation >= 386 MB), no flush"},
+            "ms_per_block": ms, "frac_of_fp4_peak": value / world / peak_fp4,
+            "flops_per_block": {"total": total, "base_fp4": base, "lora_down": ldown, "lora_up": lup},
+            "kernel_ms": {"gemm": gemm_total_ms, "prepare": ms - gemm_total_ms},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": blk.launches_per_step() * a.steps, "clocks": clocks,
+            "peaks": {"kind": peak_kind, **peaks}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    a = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", a.gpus if a.gpus == 1 else 1))
+    rank = int(os.environ.get("RANK", 0))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if world > 1 and a.impl == "native":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        if a.impl == "reference":
+            return reference_arm(a, rank, world)
+        return native_arm(a, rank, world, local_rank)
+    finally:
+        if world > 1 and a.impl == "native":
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

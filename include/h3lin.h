@@ -64,6 +64,10 @@ typedef int32_t h3lin_status;
 #define H3LIN_E_TIMEOUT     6  /* device-side bounded wait expired (device status)    */
 #define H3LIN_E_UNSUPPORTED 7  /* device is not compute capability 10.x (tcgen05)     */
 
+/* Output element types of h3lin_forward. */
+#define H3LIN_OUT_BF16      0  /* bf16, round to nearest even (the model's dtype)         */
+#define H3LIN_OUT_F32       1  /* fp32: the epilogue value before the bf16 rounding       */
+
 /* Epilogues of h3lin_forward. */
 #define H3LIN_EPI_NONE      0  /* out[M, N] = y                                       */
 #define H3LIN_EPI_SILU_MUL  1  /* y = [gate | up] (N = 2 * Nh); out[M, Nh] = silu(gate) * up */
@@ -140,7 +144,10 @@ h3lin_status h3lin_pack_weight(const void* w, int64_t N, int64_t K,
  *                    path, whose output is bit-identical to adapter == NULL
  *                    (TURBO.md, "Validation": disabled exactness).
  *   strength         finite float
- *   out              device bf16 [M, N] (SiLU*up: [M, N/2]); rows >= M untouched
+ *   out              device [M, N] (SiLU*up: [M, N/2]) of type out_dtype, row-major;
+ *                    rows >= M are never touched
+ *   out_dtype        H3LIN_OUT_BF16 or H3LIN_OUT_F32 (the bf16 output is exactly
+ *                    the round-to-nearest-even of the fp32 one)
  *   workspace        device, >= h3lin_forward_workspace_bytes(M, K, N, rank),
  *                    initialised once with h3lin_workspace_init
  * Kernels (stream order): amax pass (fused with A(x) when the adapter is
@@ -149,8 +156,22 @@ h3lin_status h3lin_pack_weight(const void* w, int64_t N, int64_t K,
 h3lin_status h3lin_forward(const void* x, int64_t M, const float* pre_quant_scale,
                            const h3lin_weight* weight, int32_t epilogue,
                            const h3lin_adapter* adapter, float strength,
-                           void* out, void* workspace, size_t workspace_bytes,
+                           void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream);
+
+/* The two stages of h3lin_forward, for callers that schedule them apart
+ * (h3lin_forward == h3lin_forward_prepare followed by h3lin_forward_gemm on
+ * the same stream).  Both must be given the same M, weight, adapter, strength
+ * and workspace; the GEMM stage reads what the prepare stage left in the
+ * workspace (quantised activation, tensor scale, A(x), scaled B).
+ *   prepare  amax pass (+ A(x) when the adapter is active) and quantise pass
+ *   gemm     FP4 GEMM + B(A(x)) into the same accumulator + epilogue */
+h3lin_status h3lin_forward_prepare(const void* x, int64_t M, const float* pre_quant_scale,
+                                   const h3lin_weight* weight, const h3lin_adapter* adapter, float strength,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+h3lin_status h3lin_forward_gemm(int64_t M, const h3lin_weight* weight, int32_t epilogue,
+                                const h3lin_adapter* adapter, float strength, void* out, int32_t out_dtype,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ status */
 /* Synchronises `stream`, then reads the workspace's sticky device status word

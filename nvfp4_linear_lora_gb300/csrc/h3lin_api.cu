@@ -136,6 +136,134 @@ h3lin_status quantize_impl(const void* x, int64_t M, int64_t K, const float* pqs
   return H3LIN_OK;
 }
 
+struct ForwardCall {
+  const void* x;
+  int64_t M, K, N, rank;
+  const float* pqs;
+  const h3lin_weight* w;
+  const h3lin_adapter* adapter;
+  float strength;
+  bool lora, silu, f32out;
+  void* out;
+  uint8_t* ws;
+  ForwardLayout L;
+  DeviceInfo dev;
+};
+
+// Host-side validation shared by h3lin_forward and its two stages.  `need_x`
+// / `need_out` say which side of the call is being checked.
+h3lin_status validate_forward(const void* x, int64_t M, const float* pqs, const h3lin_weight* w, int32_t epilogue,
+                              const h3lin_adapter* adapter, float strength, void* out, int32_t out_dtype, void* ws,
+                              size_t ws_bytes, bool need_x, bool need_out, ForwardCall* c) {
+  if ((need_x && !x) || !w || (need_out && !out) || !ws) return H3LIN_E_INVALID;
+  if (!w->codes || !w->scales || !w->tensor_scale) return H3LIN_E_INVALID;
+  if (epilogue != H3LIN_EPI_NONE && epilogue != H3LIN_EPI_SILU_MUL) return H3LIN_E_INVALID;
+  if (out_dtype != H3LIN_OUT_BF16 && out_dtype != H3LIN_OUT_F32) return H3LIN_E_INVALID;
+  if (!std::isfinite(strength)) return H3LIN_E_INVALID;
+  const int64_t K = w->K, N = w->N;
+  const bool silu = epilogue == H3LIN_EPI_SILU_MUL;
+  if (M < 1 || M > kMaxDim || K < 64 || K > kMaxK || K % 64 != 0 || N < 128 || N > kMaxDim || N % 128 != 0)
+    return H3LIN_E_SHAPE;
+  if (silu && N % 256 != 0) return H3LIN_E_SHAPE;
+  if ((need_x && !aligned16(x)) || (need_out && !aligned16(out)) || !aligned16(ws) || !aligned16(w->codes) ||
+      !aligned16(w->scales) || (pqs && !aligned16(pqs)) || (reinterpret_cast<uintptr_t>(w->tensor_scale) & 3u))
+    return H3LIN_E_ALIGN;
+  const bool lora = adapter != nullptr && strength != 0.0f;
+  int64_t rank = 0;
+  if (lora) {
+    if (!adapter->A || !adapter->B) return H3LIN_E_INVALID;
+    if (!std::isfinite(adapter->alpha)) return H3LIN_E_INVALID;
+    rank = adapter->rank;
+    if (!rank_ok(rank)) return H3LIN_E_SHAPE;
+    if (!aligned16(adapter->A) || !aligned16(adapter->B)) return H3LIN_E_ALIGN;
+  }
+  c->L = forward_layout(M, K, N, rank);
+  if (ws_bytes < c->L.total) return H3LIN_E_WORKSPACE;
+  h3lin_status s = require_device(&c->dev);
+  if (s != H3LIN_OK) return s;
+  c->x = x;
+  c->M = M;
+  c->K = K;
+  c->N = N;
+  c->rank = rank;
+  c->pqs = pqs;
+  c->w = w;
+  c->adapter = adapter;
+  c->strength = strength;
+  c->lora = lora;
+  c->silu = silu;
+  c->f32out = out_dtype == H3LIN_OUT_F32;
+  c->out = out;
+  c->ws = static_cast<uint8_t*>(ws);
+  return H3LIN_OK;
+}
+
+// amax pass (fused with u = A(x) when the adapter is active) + quantise pass.
+h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
+  uint32_t* status = reinterpret_cast<uint32_t*>(c.ws + kStatusOffset);
+  float* ts_x = reinterpret_cast<float*>(c.ws + kTsOffset);
+  float* partials = reinterpret_cast<float*>(c.ws + kPartialsOffset);
+  void* xq = c.ws + c.L.codes;
+  void* xs = c.ws + c.L.scales;
+  void* u = c.ws + c.L.u;
+  void* bp = c.ws + c.L.b;
+  const RowPlan plan = plan_rows(c.M, c.K, c.dev.sm_count);
+  int nparts = plan.blocks;
+  if (c.lora) {
+    CUtensorMap tm_x, tm_a;
+    const int a_box = c.rank <= 256 ? int(c.rank) : int(c.rank / 2);
+    if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, c.K, c.M, c.K * 2, 64, 128)) return H3LIN_E_CUDA;
+    if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.adapter->A, c.K, c.rank, c.K * 2, 64, a_box))
+      return H3LIN_E_CUDA;
+    if (launch_amax_lora(tm_x, tm_a, int(c.M), int(c.K), int(c.rank), a_box, c.pqs, partials, u, status,
+                         c.dev.sm_count, &nparts, stream) != cudaSuccess)
+      return H3LIN_E_CUDA;
+  } else {
+    if (launch_amax(c.x, int(c.M), int(c.K), c.pqs, partials, plan, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  }
+  const float lora_k = c.lora ? c.strength * (c.adapter->alpha / float(c.rank)) : 0.0f;
+  if (launch_quant(c.x, int(c.M), int(c.K), c.pqs, partials, nparts, xq, xs, ts_x, plan,
+                   c.lora ? c.adapter->B : nullptr, c.lora ? bp : nullptr, c.lora ? c.N * c.rank : 0, lora_k,
+                   c.w->tensor_scale, stream) != cudaSuccess)
+    return H3LIN_E_CUDA;
+  return H3LIN_OK;
+}
+
+// FP4 GEMM + LoRA-up + epilogue reading the prepared workspace.
+h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream) {
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  void* xq = c.ws + c.L.codes;
+  if (!make_map(&g.tm_xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, c.K / 2, c.M, c.K / 2, 128, 128)) return H3LIN_E_CUDA;
+  if (!make_map(&g.tm_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.w->codes, c.K / 2, c.N, c.K / 2, 128, 128))
+    return H3LIN_E_CUDA;
+  if (c.lora) {
+    if (!make_map(&g.tm_u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.ws + c.L.u, c.rank, c.M, c.rank * 2, 64, 128))
+      return H3LIN_E_CUDA;
+    if (!make_map(&g.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.ws + c.L.b, c.rank, c.N, c.rank * 2, 64, 128))
+      return H3LIN_E_CUDA;
+  } else {
+    g.tm_u = g.tm_xq;  // unused by the base-only kernels
+    g.tm_b = g.tm_wq;
+  }
+  g.xs = c.ws + c.L.scales;
+  g.ws = static_cast<const uint8_t*>(c.w->scales);
+  g.ts_x = reinterpret_cast<const float*>(c.ws + kTsOffset);
+  g.ts_w = c.w->tensor_scale;
+  g.out = c.out;
+  g.M = int(c.M);
+  g.N = int(c.N);
+  g.K = int(c.K);
+  g.rank = int(c.rank);
+  g.ldo = int(c.silu ? c.N / 2 : c.N);
+  g.status = reinterpret_cast<uint32_t*>(c.ws + kStatusOffset);
+  g.lora = c.lora;
+  g.silu = c.silu;
+  g.f32out = c.f32out;
+  if (launch_fp4gemm(g, c.dev.sm_count, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  return H3LIN_OK;
+}
+
 }  // namespace
 }  // namespace h3lin
 
@@ -197,93 +325,35 @@ h3lin_status h3lin_pack_weight(const void* w, int64_t N, int64_t K, void* codes,
 }
 
 h3lin_status h3lin_forward(const void* x, int64_t M, const float* pqs, const h3lin_weight* w, int32_t epilogue,
-                           const h3lin_adapter* adapter, float strength, void* out, void* ws, size_t ws_bytes,
-                           cudaStream_t stream) {
-  // ---- validation (nothing is enqueued on error)
-  if (!x || !w || !out || !ws) return H3LIN_E_INVALID;
-  if (!w->codes || !w->scales || !w->tensor_scale) return H3LIN_E_INVALID;
-  if (epilogue != H3LIN_EPI_NONE && epilogue != H3LIN_EPI_SILU_MUL) return H3LIN_E_INVALID;
-  if (!std::isfinite(strength)) return H3LIN_E_INVALID;
-  const int64_t K = w->K, N = w->N;
-  const bool silu = epilogue == H3LIN_EPI_SILU_MUL;
-  if (M < 1 || M > kMaxDim || K < 64 || K > kMaxK || K % 64 != 0 || N < 128 || N > kMaxDim || N % 128 != 0)
-    return H3LIN_E_SHAPE;
-  if (silu && N % 256 != 0) return H3LIN_E_SHAPE;
-  if (!aligned16(x) || !aligned16(out) || !aligned16(ws) || !aligned16(w->codes) || !aligned16(w->scales) ||
-      (pqs && !aligned16(pqs)) || (reinterpret_cast<uintptr_t>(w->tensor_scale) & 3u))
-    return H3LIN_E_ALIGN;
-  const bool lora = adapter != nullptr && strength != 0.0f;
-  int64_t rank = 0;
-  if (lora) {
-    if (!adapter->A || !adapter->B) return H3LIN_E_INVALID;
-    if (!std::isfinite(adapter->alpha)) return H3LIN_E_INVALID;
-    rank = adapter->rank;
-    if (!rank_ok(rank)) return H3LIN_E_SHAPE;
-    if (!aligned16(adapter->A) || !aligned16(adapter->B)) return H3LIN_E_ALIGN;
-  }
-  const ForwardLayout L = forward_layout(M, K, N, rank);
-  if (ws_bytes < L.total) return H3LIN_E_WORKSPACE;
-  DeviceInfo d;
-  h3lin_status s = require_device(&d);
+                           const h3lin_adapter* adapter, float strength, void* out, int32_t out_dtype, void* ws,
+                           size_t ws_bytes, cudaStream_t stream) {
+  ForwardCall c;
+  h3lin_status s = validate_forward(x, M, pqs, w, epilogue, adapter, strength, out, out_dtype, ws, ws_bytes, true,
+                                    true, &c);
   if (s != H3LIN_OK) return s;
+  s = enqueue_prepare(c, stream);
+  if (s != H3LIN_OK) return s;
+  return enqueue_gemm(c, stream);
+}
 
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  uint32_t* status = reinterpret_cast<uint32_t*>(wsb + kStatusOffset);
-  float* ts_x = reinterpret_cast<float*>(wsb + kTsOffset);
-  float* partials = reinterpret_cast<float*>(wsb + kPartialsOffset);
-  void* xq = wsb + L.codes;
-  void* xs = wsb + L.scales;
-  void* u = wsb + L.u;
-  void* bp = wsb + L.b;
+h3lin_status h3lin_forward_prepare(const void* x, int64_t M, const float* pqs, const h3lin_weight* w,
+                                   const h3lin_adapter* adapter, float strength, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream) {
+  ForwardCall c;
+  h3lin_status s = validate_forward(x, M, pqs, w, H3LIN_EPI_NONE, adapter, strength, nullptr, H3LIN_OUT_BF16, ws,
+                                    ws_bytes, true, false, &c);
+  if (s != H3LIN_OK) return s;
+  return enqueue_prepare(c, stream);
+}
 
-  GemmArgs g;
-  std::memset(&g, 0, sizeof(g));
-  // ---- tensor maps
-  if (!make_map(&g.tm_xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, K / 2, M, K / 2, 128, 128)) return H3LIN_E_CUDA;
-  if (!make_map(&g.tm_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, 128)) return H3LIN_E_CUDA;
-  CUtensorMap tm_x, tm_a;
-  int a_box = 0;
-  if (lora) {
-    a_box = rank <= 256 ? int(rank) : int(rank / 2);
-    if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, 128)) return H3LIN_E_CUDA;
-    if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, adapter->A, K, rank, K * 2, 64, a_box))
-      return H3LIN_E_CUDA;
-    if (!make_map(&g.tm_u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, rank, M, rank * 2, 64, 128)) return H3LIN_E_CUDA;
-    if (!make_map(&g.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, bp, rank, N, rank * 2, 64, 128)) return H3LIN_E_CUDA;
-  } else {
-    g.tm_u = g.tm_xq;  // unused by the base-only kernels
-    g.tm_b = g.tm_wq;
-  }
-
-  // ---- kernels
-  const RowPlan plan = plan_rows(M, K, d.sm_count);
-  int nparts = plan.blocks;
-  if (lora) {
-    if (launch_amax_lora(tm_x, tm_a, int(M), int(K), int(rank), a_box, pqs, partials, u, status, d.sm_count,
-                         &nparts, stream) != cudaSuccess)
-      return H3LIN_E_CUDA;
-  } else {
-    if (launch_amax(x, int(M), int(K), pqs, partials, plan, stream) != cudaSuccess) return H3LIN_E_CUDA;
-  }
-  const float lora_k = lora ? strength * (adapter->alpha / float(rank)) : 0.0f;
-  if (launch_quant(x, int(M), int(K), pqs, partials, nparts, xq, xs, ts_x, plan, lora ? adapter->B : nullptr,
-                   lora ? bp : nullptr, lora ? N * rank : 0, lora_k, w->tensor_scale, stream) != cudaSuccess)
-    return H3LIN_E_CUDA;
-  g.xs = static_cast<const uint8_t*>(xs);
-  g.ws = static_cast<const uint8_t*>(w->scales);
-  g.ts_x = ts_x;
-  g.ts_w = w->tensor_scale;
-  g.out = out;
-  g.M = int(M);
-  g.N = int(N);
-  g.K = int(K);
-  g.rank = int(rank);
-  g.ldo = int(silu ? N / 2 : N);
-  g.status = status;
-  g.lora = lora;
-  g.silu = silu;
-  if (launch_fp4gemm(g, d.sm_count, stream) != cudaSuccess) return H3LIN_E_CUDA;
-  return H3LIN_OK;
+h3lin_status h3lin_forward_gemm(int64_t M, const h3lin_weight* w, int32_t epilogue, const h3lin_adapter* adapter,
+                                float strength, void* out, int32_t out_dtype, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
+  ForwardCall c;
+  h3lin_status s = validate_forward(nullptr, M, nullptr, w, epilogue, adapter, strength, out, out_dtype, ws,
+                                    ws_bytes, false, true, &c);
+  if (s != H3LIN_OK) return s;
+  return enqueue_gemm(c, stream);
 }
 
 h3lin_status h3lin_read_status(const void* ws, cudaStream_t stream, int32_t* device_status) {

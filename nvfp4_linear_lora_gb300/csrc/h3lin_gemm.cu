@@ -4,7 +4,7 @@
 //   acc[m, n]  = sum_k E2M1(xq) E4M3(sx) * E2M1(wq) E4M3(sw)   (FP4 tensor cores)
 //   acc[m, n] += sum_j u[m, j] * B'[n, j]                        (BF16 tensor cores)
 //   y          = ts_x * ts_w * acc                               (B' carries 1/(ts_x ts_w))
-//   out        = y, or silu(y_gate) * y_up                       (bf16, rows >= M masked)
+//   out        = y, or silu(y_gate) * y_up                       (bf16 or fp32, rows >= M masked)
 //
 // This is `NVFP4_base(x) + strength * (alpha/rank) * B(A(x))` of TURBO.md
 // (h3-blackwell-runtime, "Implementation") with the fused gate/up SiLU*up of
@@ -51,12 +51,29 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 
 __device__ __forceinline__ float silu(float g) { return g * __frcp_rn(1.0f + __expf(-g)); }
 
-template <int BN, bool SILU, bool LORA>
+// Store 8 consecutive epilogue values of one row: bf16 (16 bytes) or fp32 (32 bytes).
+template <bool F32OUT>
+__device__ __forceinline__ void store8(void* out_row, int col, const float (&h)[8]) {
+  if (F32OUT) {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(out_row) + col);
+    d[0] = make_float4(h[0], h[1], h[2], h[3]);
+    d[1] = make_float4(h[4], h[5], h[6], h[7]);
+  } else {
+    uint4 o;
+    o.x = pack_bf16x2(h[0], h[1]);
+    o.y = pack_bf16x2(h[2], h[3]);
+    o.z = pack_bf16x2(h[4], h[5]);
+    o.w = pack_bf16x2(h[6], h[7]);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_row) + col) = o;
+  }
+}
+
+template <int BN, bool SILU, bool LORA, bool F32OUT>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
     const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_wq,
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_b,
     const uint8_t* __restrict__ xs, const uint8_t* __restrict__ ws, const float* __restrict__ ts_x,
-    const float* __restrict__ ts_w, __nv_bfloat16* __restrict__ out, int M, int N, int K, int rank, int ldo,
+    const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K, int rank, int ldo,
     uint32_t* __restrict__ status) {
   using C = GemmCfg<BN>;
   static_assert(!SILU || BN == 256, "SiLU*up pairs 128 gate and 128 up columns");
@@ -241,8 +258,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
       if (lane == 0) mbar_arrive(tmem_empty);
       acc_ph ^= 1;
       if (row < M) {
+        void* out_row = static_cast<uint8_t*>(out) + static_cast<int64_t>(row) * ldo * (F32OUT ? 4 : 2);
         if (SILU) {
-          uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(row) * ldo + tn * 128 + half * 64);
+          const int col0 = tn * 128 + half * 64;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
 #pragma unroll
@@ -254,30 +272,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
                 const float u = __fmul_rn(scale, __uint_as_float(v[2 + i][8 * w + e]));
                 hv[e] = __fmul_rn(silu(g), u);
               }
-              uint4 o;
-              o.x = pack_bf16x2(hv[0], hv[1]);
-              o.y = pack_bf16x2(hv[2], hv[3]);
-              o.z = pack_bf16x2(hv[4], hv[5]);
-              o.w = pack_bf16x2(hv[6], hv[7]);
-              dst[4 * i + w] = o;
+              store8<F32OUT>(out_row, col0 + 32 * i + 8 * w, hv);
             }
           }
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(row) * ldo + tn * BN + half * (BN / 2));
+          const int col0 = tn * BN + half * (BN / 2);
 #pragma unroll
           for (int i = 0; i < kChunks; ++i) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-              uint4 o;
-              o.x = pack_bf16x2(__fmul_rn(scale, __uint_as_float(v[i][8 * w + 0])),
-                                __fmul_rn(scale, __uint_as_float(v[i][8 * w + 1])));
-              o.y = pack_bf16x2(__fmul_rn(scale, __uint_as_float(v[i][8 * w + 2])),
-                                __fmul_rn(scale, __uint_as_float(v[i][8 * w + 3])));
-              o.z = pack_bf16x2(__fmul_rn(scale, __uint_as_float(v[i][8 * w + 4])),
-                                __fmul_rn(scale, __uint_as_float(v[i][8 * w + 5])));
-              o.w = pack_bf16x2(__fmul_rn(scale, __uint_as_float(v[i][8 * w + 6])),
-                                __fmul_rn(scale, __uint_as_float(v[i][8 * w + 7])));
-              dst[4 * i + w] = o;
+              float hv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) hv[e] = __fmul_rn(scale, __uint_as_float(v[i][8 * w + e]));
+              store8<F32OUT>(out_row, col0 + 32 * i + 8 * w, hv);
             }
           }
         }
@@ -292,10 +299,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
   }
 }
 
-template <int BN, bool SILU, bool LORA>
+template <int BN, bool SILU, bool LORA, bool F32OUT>
 static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t st) {
   using C = GemmCfg<BN>;
-  auto kern = k_fp4gemm<BN, SILU, LORA>;
+  auto kern = k_fp4gemm<BN, SILU, LORA, F32OUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const int tiles_m = (a.M + 127) / 128;
@@ -303,22 +310,27 @@ static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t 
   const int tiles = tiles_m * tiles_n;
   const int grid = tiles < sm_count ? tiles : sm_count;
   kern<<<grid, kGemmThreads, C::kSmem, st>>>(a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.xs, a.ws, a.ts_x, a.ts_w,
-                                             static_cast<__nv_bfloat16*>(a.out), a.M, a.N, a.K, a.rank, a.ldo,
+                                             a.out, a.M, a.N, a.K, a.rank, a.ldo,
                                              a.status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st) {
+template <bool F32OUT>
+static cudaError_t launch_dtype(const GemmArgs& a, int sm_count, cudaStream_t st) {
   if (a.silu) {
-    return a.lora ? launch_variant<256, true, true>(a, sm_count, st)
-                  : launch_variant<256, true, false>(a, sm_count, st);
+    return a.lora ? launch_variant<256, true, true, F32OUT>(a, sm_count, st)
+                  : launch_variant<256, true, false, F32OUT>(a, sm_count, st);
   }
   if (a.N % 256 == 0) {
-    return a.lora ? launch_variant<256, false, true>(a, sm_count, st)
-                  : launch_variant<256, false, false>(a, sm_count, st);
+    return a.lora ? launch_variant<256, false, true, F32OUT>(a, sm_count, st)
+                  : launch_variant<256, false, false, F32OUT>(a, sm_count, st);
   }
-  return a.lora ? launch_variant<128, false, true>(a, sm_count, st)
-                : launch_variant<128, false, false>(a, sm_count, st);
+  return a.lora ? launch_variant<128, false, true, F32OUT>(a, sm_count, st)
+                : launch_variant<128, false, false, F32OUT>(a, sm_count, st);
+}
+
+cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st) {
+  return a.f32out ? launch_dtype<true>(a, sm_count, st) : launch_dtype<false>(a, sm_count, st);
 }
 
 }  // namespace h3lin

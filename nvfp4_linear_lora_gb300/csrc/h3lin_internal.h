@@ -50,7 +50,7 @@ struct GemmArgs {
   void* out;
   int M, N, K, rank, ldo;
   uint32_t* status;
-  bool lora, silu;
+  bool lora, silu, f32out;
 };
 cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st);
 

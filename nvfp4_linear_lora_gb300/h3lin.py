@@ -24,6 +24,8 @@ H3LIN_E_WORKSPACE = 4
 H3LIN_E_CUDA = 5
 H3LIN_E_TIMEOUT = 6
 H3LIN_E_UNSUPPORTED = 7
+H3LIN_OUT_BF16 = 0
+H3LIN_OUT_F32 = 1
 H3LIN_EPI_NONE = 0
 H3LIN_EPI_SILU_MUL = 1
 
@@ -58,7 +60,11 @@ _SIGNATURES = {
     "h3lin_quantize_act": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_pack_weight": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_forward": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), _i32, ctypes.POINTER(h3lin_adapter),
-                             _f32, _vp, _vp, _sz, _vp]),
+                             _f32, _vp, _i32, _vp, _sz, _vp]),
+    "h3lin_forward_prepare": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter),
+                                     _f32, _vp, _sz, _vp]),
+    "h3lin_forward_gemm": (_i32, [_i64, ctypes.POINTER(h3lin_weight), _i32, ctypes.POINTER(h3lin_adapter), _f32,
+                                  _vp, _i32, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
 }
 
@@ -115,10 +121,22 @@ def h3lin_pack_weight(w, N, K, codes, scales, tensor_scale, ws, ws_bytes, stream
     return lib().h3lin_pack_weight(w, N, K, codes, scales, tensor_scale, ws, ws_bytes, stream)
 
 
-def h3lin_forward(x, M, pqs, weight, epilogue, adapter, strength, out, ws, ws_bytes, stream):
+def h3lin_forward(x, M, pqs, weight, epilogue, adapter, strength, out, out_dtype, ws, ws_bytes, stream):
     wp = ctypes.byref(weight) if weight is not None else None
     ap = ctypes.byref(adapter) if adapter is not None else None
-    return lib().h3lin_forward(x, M, pqs, wp, epilogue, ap, strength, out, ws, ws_bytes, stream)
+    return lib().h3lin_forward(x, M, pqs, wp, epilogue, ap, strength, out, out_dtype, ws, ws_bytes, stream)
+
+
+def h3lin_forward_prepare(x, M, pqs, weight, adapter, strength, ws, ws_bytes, stream):
+    wp = ctypes.byref(weight) if weight is not None else None
+    ap = ctypes.byref(adapter) if adapter is not None else None
+    return lib().h3lin_forward_prepare(x, M, pqs, wp, ap, strength, ws, ws_bytes, stream)
+
+
+def h3lin_forward_gemm(M, weight, epilogue, adapter, strength, out, out_dtype, ws, ws_bytes, stream):
+    wp = ctypes.byref(weight) if weight is not None else None
+    ap = ctypes.byref(adapter) if adapter is not None else None
+    return lib().h3lin_forward_gemm(M, wp, epilogue, ap, strength, out, out_dtype, ws, ws_bytes, stream)
 
 
 def h3lin_read_status(ws, stream):
@@ -207,13 +225,17 @@ def pack_weight(w, workspace=None):
 
 
 def forward(x, weight, pre_quant_scale=None, adapter=None, strength=1.0, silu_mul=False, out=None,
-            workspace=None):
-    """One projection through ``h3lin_forward``; returns ``out`` (bf16)."""
+            workspace=None, out_dtype=None):
+    """One projection through ``h3lin_forward``; returns ``out`` (bf16 unless
+    ``out_dtype``/``out`` say float32)."""
     torch = _torch()
     M = x.shape[0]
     n_out = weight.N // 2 if silu_mul else weight.N
     if out is None:
-        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((M, n_out), dtype=out_dtype or torch.bfloat16, device=x.device)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    code = H3LIN_OUT_F32 if out.dtype == torch.float32 else H3LIN_OUT_BF16
     if workspace is None:
         workspace = new_workspace(h3lin_forward_workspace_bytes(M, weight.K, weight.N,
                                                                 adapter.rank if adapter else 0), x.device)
@@ -221,7 +243,7 @@ def forward(x, weight, pre_quant_scale=None, adapter=None, strength=1.0, silu_mu
     ac = adapter.c_struct() if adapter is not None else None
     _check(h3lin_forward(x.data_ptr(), M, _ptr(pre_quant_scale), wc,
                          H3LIN_EPI_SILU_MUL if silu_mul else H3LIN_EPI_NONE, ac, float(strength),
-                         out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream()), "h3lin_forward")
+                         out.data_ptr(), code, workspace.data_ptr(), workspace.numel(), _stream()), "h3lin_forward")
     return out
 
 

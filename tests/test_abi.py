@@ -63,12 +63,12 @@ def _weight(N=384, K=256):
 
 
 def _fwd(**kw):
-    args = dict(x=A, M=200, pqs=None, weight=_weight(), epilogue=0, adapter=None, strength=1.0, out=A, ws=A,
-                ws_bytes=1 << 30, stream=None)
+    args = dict(x=A, M=200, pqs=None, weight=_weight(), epilogue=0, adapter=None, strength=1.0, out=A,
+                out_dtype=0, ws=A, ws_bytes=1 << 30, stream=None)
     args.update(kw)
     return h3lin.h3lin_forward(args["x"], args["M"], args["pqs"], args["weight"], args["epilogue"],
-                               args["adapter"], args["strength"], args["out"], args["ws"], args["ws_bytes"],
-                               args["stream"])
+                               args["adapter"], args["strength"], args["out"], args["out_dtype"], args["ws"],
+                               args["ws_bytes"], args["stream"])
 
 
 def test_forward_rejects_invalid_arguments():
@@ -77,6 +77,7 @@ def test_forward_rejects_invalid_arguments():
     assert _fwd(out=None) == E.H3LIN_E_INVALID
     assert _fwd(weight=h3lin.h3lin_weight(None, A, A, 384, 256)) == E.H3LIN_E_INVALID
     assert _fwd(epilogue=7) == E.H3LIN_E_INVALID
+    assert _fwd(out_dtype=2) == E.H3LIN_E_INVALID
     assert _fwd(strength=math.nan) == E.H3LIN_E_INVALID
     assert _fwd(strength=math.inf) == E.H3LIN_E_INVALID
     assert _fwd(M=0) == E.H3LIN_E_SHAPE
