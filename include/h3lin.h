@@ -173,6 +173,29 @@ h3lin_status h3lin_forward_gemm(int64_t M, const h3lin_weight* weight, int32_t e
                                 const h3lin_adapter* adapter, float strength, void* out, int32_t out_dtype,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ----------------------------------------------- forward without allocation */
+/* No counterpart in the paper: a library-level addition.
+ *
+ * h3lin_forward for callers that cannot allocate device memory at all (for
+ * example a plugin inside a host application that owns every allocation and
+ * gives plugins no allocator, or a latency-bound loop where cudaMalloc and
+ * cudaFree are forbidden because they can block on the device).  Same
+ * arguments and results as h3lin_forward, minus the workspace: the scratch
+ * is a fixed H3LIN_NOALLOC_SCRATCH_BYTES array inside the library, one per
+ * device, held from module load until process exit.  Nothing is allocated.
+ *   - Calls whose scratch need (h3lin_forward_workspace_bytes) exceeds
+ *     H3LIN_NOALLOC_SCRATCH_BYTES return H3LIN_E_WORKSPACE, enqueueing nothing.
+ *   - All calls on a device share the array; calls that may overlap on the
+ *     GPU race on it.  Order them on one stream.
+ *   - The first call on each device looks up the array's device address;
+ *     make it before any stream capture begins.
+ *   - The device status word is internal to the array (not readable). */
+#define H3LIN_NOALLOC_SCRATCH_BYTES (64u << 20)
+h3lin_status h3lin_forward_noalloc(const void* x, int64_t M, const float* pre_quant_scale,
+                                   const h3lin_weight* weight, int32_t epilogue,
+                                   const h3lin_adapter* adapter, float strength, void* out,
+                                   int32_t out_dtype, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ status */
 /* Synchronises `stream`, then reads the workspace's sticky device status word
  * (H3LIN_OK or H3LIN_E_TIMEOUT) into *device_status.  Returns H3LIN_E_CUDA if

@@ -66,7 +66,11 @@ _SIGNATURES = {
     "h3lin_forward_gemm": (_i32, [_i64, ctypes.POINTER(h3lin_weight), _i32, ctypes.POINTER(h3lin_adapter), _f32,
                                   _vp, _i32, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+    "h3lin_forward_noalloc": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), _i32,
+                                     ctypes.POINTER(h3lin_adapter), _f32, _vp, _i32, _vp]),
 }
+
+H3LIN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def lib():
@@ -137,6 +141,14 @@ def h3lin_forward_gemm(M, weight, epilogue, adapter, strength, out, out_dtype, w
     wp = ctypes.byref(weight) if weight is not None else None
     ap = ctypes.byref(adapter) if adapter is not None else None
     return lib().h3lin_forward_gemm(M, wp, epilogue, ap, strength, out, out_dtype, ws, ws_bytes, stream)
+
+
+def h3lin_forward_noalloc(x, M, pqs, weight, epilogue, adapter, strength, out, out_dtype, stream):
+    """h3lin_forward for callers that cannot allocate: the scratch is a fixed
+    array inside the library (see include/h3lin.h for the rules)."""
+    wp = ctypes.byref(weight) if weight is not None else None
+    ap = ctypes.byref(adapter) if adapter is not None else None
+    return lib().h3lin_forward_noalloc(x, M, pqs, wp, epilogue, ap, strength, out, out_dtype, stream)
 
 
 def h3lin_read_status(ws, stream):
