@@ -77,6 +77,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Scale bytes viewed as a 2-D tensor of 256-byte rows; a box of 8 rows is
+// four 512-byte scale atoms (one pipeline stage of 128 rows x 256 K).
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t bytes) {
+  auto fn = encode_fn();
+  if (!fn || bytes % 256 != 0 || bytes < 8 * 256) return false;
+  cuuint64_t dims[2] = {256, bytes / 256};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 8};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major 2-D tensor [rows, inner] with a 128-byte-swizzled box.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
@@ -260,6 +275,10 @@ h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream) {
   g.lora = c.lora;
   g.silu = c.silu;
   g.f32out = c.f32out;
+  // CTA-pair kernel for N % 256 == 0 (and SiLU*up, whose N is a multiple of 256)
+  g.pair = (c.N % 256 == 0) && c.dev.sm_count >= 2 &&
+           make_sf_map(&g.tm_xs, g.xs, size_t((c.M + 127) / 128 * 128) * size_t(c.K / 16)) &&
+           make_sf_map(&g.tm_ws, g.ws, size_t(c.N) * size_t(c.K / 16));
   if (launch_fp4gemm(g, c.dev.sm_count, stream) != cudaSuccess) return H3LIN_E_CUDA;
   return H3LIN_OK;
 }

@@ -10,7 +10,11 @@
 // (h3-blackwell-runtime, "Implementation") with the fused gate/up SiLU*up of
 // the MiniMax-H3 Ultra Fast README ("Active optimization stack", row MLP).
 //
-// Persistent, warp-specialised, one 128 x BN tile per CTA iteration:
+// Two kernels: the CTA-pair kernel (cta_group::2, 256 x 256 tiles; used when
+// N is a multiple of 256 or for SiLU*up) and the single-CTA kernel below
+// (128 x BN tiles, BN = 128 for the remaining shapes).
+//
+// Single-CTA kernel: persistent, warp-specialised, one 128 x BN tile per CTA iteration:
 //   warp 0      TMA producer (operand tiles, block-scale atoms by bulk copy)
 //   warp 1      TMEM owner; lane 0 issues tcgen05.cp of the scales and the MMAs
 //   warps 2-9   epilogue: TMEM -> registers, release the accumulator, then
@@ -315,6 +319,345 @@ static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t 
   return cudaGetLastError();
 }
 
+
+// ============================================================ CTA-pair kernel
+// Pair tile 256 x 256: the two CTAs of a cluster each own 128 output rows and
+// issue one tcgen05 MMA of M = 256 together (cta_group::2).  Each CTA loads its
+// own 128 rows of A, 128 of the 256 B rows, the scale atoms of its A rows and
+// of all 256 B rows; every TMA load of both CTAs is counted on the leader's
+// barrier.  Warp 0: producer.  Warp 1 (leader): MMA issuer.  Warp 2 (leader):
+// copies the stage's scale atoms into TMEM (tcgen05.cp) — a separate thread,
+// so the copies overlap the previous stage's MMAs instead of queueing behind
+// them.  Warps 3-10: epilogue, staging each warp's 32 x 128-byte block through
+// shared memory so every global store writes whole 128-byte lines.
+constexpr int kPairThreads = 352;
+struct PairCfg {
+  static constexpr int kABytes = 128 * 128;
+  static constexpr int kBBytes = 128 * 128;
+  static constexpr int kSfaBytes = 4 * 512;
+  static constexpr int kSfbBytes = 2 * 4 * 512;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;   // 38 KB
+  static constexpr int kStages = 5;
+  static constexpr int kSfCols = 16 + 32;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiScratch = 4096;                                          // per epilogue warp
+  static constexpr int kSmem = kStages * kStageBytes + kEpiWarps * kEpiScratch + 1024 + 256;
+  static constexpr int kTmemCols = 512;
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(256 + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+template <bool SILU, bool LORA, bool F32OUT>
+__global__ void __launch_bounds__(kPairThreads, 1) k_fp4gemm_pair(
+    const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_wq,
+    const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_b,
+    const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_ws,
+    const float* __restrict__ ts_x, const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K,
+    int rank, int ldo, uint32_t* __restrict__ status) {
+  using C = PairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* epi_scratch = smem + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_scratch + C::kEpiWarps * C::kEpiScratch);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* sf_full = empty + C::kStages;
+  uint64_t* tmem_full = sf_full + C::kStages;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* drain_bar = tmem_empty + 1;
+  uint64_t* drain_cp = drain_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_cp + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 2 * C::kEpiWarps);
+    mbar_init(drain_bar, 1);
+    mbar_init(drain_cp, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_xq);
+    tma_prefetch_desc(&tm_wq);
+    tma_prefetch_desc(&tm_xs);
+    tma_prefetch_desc(&tm_ws);
+    if (LORA) {
+      tma_prefetch_desc(&tm_u);
+      tma_prefetch_desc(&tm_b);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, status};
+
+  const int tiles_m = (M + 255) >> 8;
+  const int tiles_n = SILU ? (N / 2) / 128 : N / 256;
+  const int num_tiles = tiles_m * tiles_n;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int nk = (K + 255) >> 8;
+  const int nr = LORA ? (rank + 63) >> 6 : 0;
+  const int k_atoms = K >> 6;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      for (int t = pair; t < num_tiles; t += npairs) {
+        int tm, tn;
+        tile_coords(t, tiles_m, tiles_n, tm, tn);
+        const int m0 = tm * 256 + 128 * static_cast<int>(crank);
+        const int h0 = SILU ? tn * 128 : tn * 256;              // B rows of the tile's two halves
+        const int h1 = SILU ? N / 2 + tn * 128 : tn * 256 + 128;
+        const int brow = crank ? h1 : h0;                        // this CTA's half
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
+          uint8_t* base = smem + st * C::kStageBytes;
+          const uint32_t lbar = cluster_addr(&full[st], 0);
+          if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::kStageBytes);
+          tma_load_2d_pair(base, &tm_xq, lbar, kc * 128, m0);
+          tma_load_2d_pair(base + C::kABytes, &tm_wq, lbar, kc * 128, brow);
+          tma_load_2d_pair(base + C::kABytes + C::kBBytes, &tm_xs, lbar, 0, 2 * ((m0 >> 7) * k_atoms + kc * 4));
+          tma_load_2d_pair(base + C::kABytes + C::kBBytes + C::kSfaBytes, &tm_ws, lbar, 0,
+                           2 * ((h0 >> 7) * k_atoms + kc * 4));
+          tma_load_2d_pair(base + C::kABytes + C::kBBytes + C::kSfaBytes + 2048, &tm_ws, lbar, 0,
+                           2 * ((h1 >> 7) * k_atoms + kc * 4));
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+        for (int rc = 0; rc < nr; ++rc) {
+          if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
+          uint8_t* base = smem + st * C::kStageBytes;
+          const uint32_t lbar = cluster_addr(&full[st], 0);
+          if (leader) mbar_arrive_expect_tx(&full[st], 2 * (C::kABytes + C::kBBytes));
+          tma_load_2d_pair(base, &tm_u, lbar, rc * 64, m0);
+          tma_load_2d_pair(base + C::kABytes, &tm_b, lbar, rc * 64, brow);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && leader) {
+      int st = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      const uint32_t idesc_f4 = idesc_nvfp4_m256(256);
+      const uint32_t idesc_bf = idesc_bf16_m256(256);
+      for (int t = pair; t < num_tiles; t += npairs) {
+        if (!mbar_wait(tmem_empty, acc_ph ^ 1, ab)) goto mma_done;
+        tc_fence_after();
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&full[st], ph, ab) || !mbar_wait(&sf_full[st], ph, ab)) goto mma_done;
+          tc_fence_after();
+          const int nsub = min(4, (K - kc * 256) >> 6);
+          const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
+          const uint32_t b_addr = a_addr + C::kABytes;
+          const uint32_t sf_col = tmem + 256 + st * C::kSfCols;
+          for (int j = 0; j < nsub; ++j)
+            mma_nvfp4_pair(tmem, sdesc_kmajor_sw128(a_addr + j * 32), sdesc_kmajor_sw128(b_addr + j * 32), idesc_f4,
+                           sf_col + 4 * j, sf_col + 16 + 8 * j, (kc | j) != 0);
+          tc_commit_pair_mc(&empty[st]);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+        for (int rc = 0; rc < nr; ++rc) {
+          if (!mbar_wait(&full[st], ph, ab) || !mbar_wait(&sf_full[st], ph, ab)) goto mma_done;
+          tc_fence_after();
+          const int nk16 = min(4, (rank - rc * 64) >> 4);
+          const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
+          const uint32_t b_addr = a_addr + C::kABytes;
+          for (int j = 0; j < nk16; ++j)
+            mma_bf16_pair(tmem, sdesc_kmajor_sw128(a_addr + j * 32), sdesc_kmajor_sw128(b_addr + j * 32), idesc_bf, 1u);
+          tc_commit_pair_mc(&empty[st]);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+        tc_commit_pair_mc(tmem_full);
+        acc_ph ^= 1;
+      }
+    mma_done:
+      tc_commit_pair(drain_bar);
+      mbar_drain(drain_bar, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- scale atoms -> TMEM
+    if (lane == 0 && leader) {
+      int st = 0;
+      uint32_t ph = 0;
+      for (int t = pair; t < num_tiles; t += npairs) {
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&full[st], ph, ab)) goto cp_done;
+          tc_fence_after();
+          const int nsub = min(4, (K - kc * 256) >> 6);
+          const uint32_t sfa_addr = smem_u32(smem + st * C::kStageBytes) + C::kABytes + C::kBBytes;
+          const uint32_t sfb_addr = sfa_addr + C::kSfaBytes;
+          const uint32_t sf_col = tmem + 256 + st * C::kSfCols;
+          for (int j = 0; j < nsub; ++j) {
+            tmem_cp_sf_atom_pair(sf_col + 4 * j, sdesc_sf_atom(sfa_addr + j * 512));
+            tmem_cp_sf_atom_pair(sf_col + 16 + 8 * j, sdesc_sf_atom(sfb_addr + j * 512));
+            tmem_cp_sf_atom_pair(sf_col + 16 + 8 * j + 4, sdesc_sf_atom(sfb_addr + 2048 + j * 512));
+          }
+          tc_commit_pair(&sf_full[st]);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+        for (int rc = 0; rc < nr; ++rc) {   // LoRA stages carry no scales
+          if (!mbar_wait(&full[st], ph, ab)) goto cp_done;
+          tc_commit_pair(&sf_full[st]);
+          if (++st == C::kStages) { st = 0; ph ^= 1; }
+        }
+      }
+    cp_done:
+      tc_commit_pair(drain_cp);
+      mbar_drain(drain_cp, 0);
+    }
+  } else if (warp < 3 + C::kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int e = warp - 3;
+    const int half = e >> 2;                 // which half of the tile's columns
+    uint8_t* scratch = epi_scratch + e * C::kEpiScratch;
+    const float scale = __fmul_rn(*ts_x, *ts_w);
+    const uint32_t leader_tmem_empty = cluster_addr(tmem_empty, 0);
+    constexpr int kEsize = F32OUT ? 4 : 2;
+    constexpr int kColsPerPass = 128 / kEsize;            // 128-byte row segment per pass
+    constexpr int kOutCols = SILU ? 64 : 128;             // output columns of this warp
+    constexpr int kPasses = kOutCols / kColsPerPass;
+    uint32_t acc_ph = 0;
+    for (int t = pair; t < num_tiles; t += npairs) {
+      int tm, tn;
+      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      if (!mbar_wait(tmem_full, acc_ph, ab)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      uint32_t v[4][32];
+      if (SILU) {
+        tmem_ld32(taddr + half * 64, v[0]);
+        tmem_ld32(taddr + half * 64 + 32, v[1]);
+        tmem_ld32(taddr + 128 + half * 64, v[2]);
+        tmem_ld32(taddr + 128 + half * 64 + 32, v[3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_ld32(taddr + half * 128 + 32 * i, v[i]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+      acc_ph ^= 1;
+
+      const int row0 = tm * 256 + 128 * static_cast<int>(crank) + 32 * q;   // first row of this warp
+      const int col0 = SILU ? tn * 128 + half * 64 : tn * 256 + half * 128;
+      const int64_t row_bytes = static_cast<int64_t>(ldo) * kEsize;
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        // this thread's row segment (128 bytes) -> swizzled scratch row `lane`, 16 bytes at a time
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (F32OUT) {
+              const int col = p * 32 + 4 * c + i;
+              float h;
+              if (SILU) {
+                const float g = __fmul_rn(scale, __uint_as_float(v[col >> 5][col & 31]));
+                const float u = __fmul_rn(scale, __uint_as_float(v[2 + (col >> 5)][col & 31]));
+                h = __fmul_rn(silu(g), u);
+              } else {
+                h = __fmul_rn(scale, __uint_as_float(v[col >> 5][col & 31]));
+              }
+              w[i] = __float_as_uint(h);
+            } else {
+              float h2[2];
+#pragma unroll
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const int col = p * 64 + 8 * c + 2 * i + k2;
+                if (SILU) {
+                  const float g = __fmul_rn(scale, __uint_as_float(v[col >> 5][col & 31]));
+                  const float u = __fmul_rn(scale, __uint_as_float(v[2 + (col >> 5)][col & 31]));
+                  h2[k2] = __fmul_rn(silu(g), u);
+                } else {
+                  h2[k2] = __fmul_rn(scale, __uint_as_float(v[col >> 5][col & 31]));
+                }
+              }
+              w[i] = pack_bf16x2(h2[0], h2[1]);
+            }
+          }
+          *reinterpret_cast<uint4*>(scratch + lane * 128 + ((c ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncwarp();
+        // 4 rows x 128 contiguous bytes per store instruction
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = it * 4 + (lane >> 3);
+          const int c = lane & 7;
+          const uint4 val = *reinterpret_cast<const uint4*>(scratch + r * 128 + ((c ^ (r & 7)) << 4));
+          if (row0 + r < M) {
+            uint8_t* dst = static_cast<uint8_t*>(out) + static_cast<int64_t>(row0 + r) * row_bytes +
+                           static_cast<int64_t>(col0 + p * kColsPerPass) * kEsize + c * 16;
+            *reinterpret_cast<uint4*>(dst) = val;
+          }
+        }
+        __syncwarp();
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+}
+
+template <bool SILU, bool LORA, bool F32OUT>
+static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStream_t st) {
+  auto kern = k_fp4gemm_pair<SILU, LORA, F32OUT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
+  if (e != cudaSuccess) return e;
+  const int tiles_m = (a.M + 255) / 256;
+  const int tiles_n = SILU ? (a.N / 2) / 128 : a.N / 256;
+  const int tiles = tiles_m * tiles_n;
+  const int max_pairs = sm_count / 2;
+  const int grid = 2 * (tiles < max_pairs ? tiles : max_pairs);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.tm_xs, a.tm_ws, a.ts_x, a.ts_w, a.out,
+                            a.M, a.N, a.K, a.rank, a.ldo, a.status);
+}
+
+template <bool F32OUT>
+static cudaError_t launch_pair_dtype(const GemmArgs& a, int sm_count, cudaStream_t st) {
+  if (a.silu) {
+    return a.lora ? launch_pair_variant<true, true, F32OUT>(a, sm_count, st)
+                  : launch_pair_variant<true, false, F32OUT>(a, sm_count, st);
+  }
+  return a.lora ? launch_pair_variant<false, true, F32OUT>(a, sm_count, st)
+                : launch_pair_variant<false, false, F32OUT>(a, sm_count, st);
+}
+
 template <bool F32OUT>
 static cudaError_t launch_dtype(const GemmArgs& a, int sm_count, cudaStream_t st) {
   if (a.silu) {
@@ -330,6 +673,7 @@ static cudaError_t launch_dtype(const GemmArgs& a, int sm_count, cudaStream_t st
 }
 
 cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st) {
+  if (a.pair) return a.f32out ? launch_pair_dtype<true>(a, sm_count, st) : launch_pair_dtype<false>(a, sm_count, st);
   return a.f32out ? launch_dtype<true>(a, sm_count, st) : launch_dtype<false>(a, sm_count, st);
 }
 

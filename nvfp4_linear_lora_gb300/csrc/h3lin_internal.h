@@ -43,6 +43,7 @@ cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, i
 // FP4 GEMM + optional LoRA-up + epilogue.
 struct GemmArgs {
   CUtensorMap tm_xq, tm_wq, tm_u, tm_b;
+  CUtensorMap tm_xs, tm_ws;   // scale bytes viewed as [bytes / 256, 256] (pair kernel)
   const uint8_t* xs;
   const uint8_t* ws;
   const float* ts_x;
@@ -51,6 +52,7 @@ struct GemmArgs {
   int M, N, K, rank, ldo;
   uint32_t* status;
   bool lora, silu, f32out;
+  bool pair;                  // use the CTA-pair kernel
 };
 cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st);
 
