@@ -325,22 +325,33 @@ static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t 
 // issue one tcgen05 MMA of M = 256 together (cta_group::2).  Each CTA loads its
 // own 128 rows of A, 128 of the 256 B rows, the scale atoms of its A rows and
 // of all 256 B rows; every TMA load of both CTAs is counted on the leader's
-// barrier.  Warp 0: producer.  Warp 1 (leader): MMA issuer.  Warp 2 (leader):
-// copies the stage's scale atoms into TMEM (tcgen05.cp) — a separate thread,
-// so the copies overlap the previous stage's MMAs instead of queueing behind
-// them.  Warps 3-10: epilogue, staging each warp's 32 x 128-byte block through
-// shared memory so every global store writes whole 128-byte lines.
-constexpr int kPairThreads = 352;
+// barrier.
+//   warp 0        producer
+//   warp 1        (leader) MMA issuer
+//   warps 2-7     (leader) scale atoms -> TMEM, two tcgen05.cp each per stage:
+//                 a copy costs its issuing thread a long issue slot, so six
+//                 issuing warps keep the twelve copies of a stage off the
+//                 critical path (they overlap the previous stage's MMAs)
+//   warps 8-15    epilogue: drain TMEM 32 columns at a time into a per-warp
+//                 shared scratch (already scaled / SiLU*up / packed), release
+//                 the accumulator, then store whole 128-byte lines
+// Copy warps: six for plain tiles; four for SiLU*up tiles, whose epilogue
+// keeps all 128 accumulator columns in registers (more registers per thread).
+template <bool SILU> struct PairRoles {
+  static constexpr int kCpWarps = SILU ? 4 : 6;
+  static constexpr int kEpiWarp0 = 2 + kCpWarps;
+  static constexpr int kThreads = 32 * (kEpiWarp0 + 8);
+};
 struct PairCfg {
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = 128 * 128;
   static constexpr int kSfaBytes = 4 * 512;
   static constexpr int kSfbBytes = 2 * 4 * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;   // 38 KB
-  static constexpr int kStages = 5;
+  static constexpr int kStages = 4;
   static constexpr int kSfCols = 16 + 32;
   static constexpr int kEpiWarps = 8;
-  static constexpr int kEpiScratch = 4096;                                          // per epilogue warp
+  static constexpr int kEpiScratch = 8192;                                          // 32 rows x 256 bytes
   static constexpr int kSmem = kStages * kStageBytes + kEpiWarps * kEpiScratch + 1024 + 256;
   static constexpr int kTmemCols = 512;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -348,14 +359,41 @@ struct PairCfg {
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
+// silu(g) * u with g = scale * acc_gate, u = scale * acc_up (fast exp and divide;
+// for very negative g the quotient underflows to 0, the limit of g / (1 + e^-g)).
+__device__ __forceinline__ float silu_mul_fast(float scale, uint32_t acc_g, uint32_t acc_u) {
+  const float g = __fmul_rn(scale, __uint_as_float(acc_g));
+  const float u = __fmul_rn(scale, __uint_as_float(acc_u));
+  return __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
+}
+
+// Store the warp's scratch (32 rows x `row_bytes` bytes, 16-byte chunks swizzled
+// by row) to global rows row0.. with whole-line stores; rows >= M skipped.
+template <int kRowBytes>
+__device__ __forceinline__ void epi_flush(const uint8_t* scratch, uint8_t* out, int64_t out_row_bytes, int row0,
+                                          int M, int lane) {
+  constexpr int kChunks = kRowBytes / 16;          // 16-byte chunks per row
+  constexpr int kRowsPerStep = 32 / kChunks;       // rows written by one warp-wide store
+#pragma unroll
+  for (int it = 0; it < 32 / kRowsPerStep; ++it) {
+    const int r = it * kRowsPerStep + lane / kChunks;
+    const int c = lane % kChunks;
+    const uint4 val = *reinterpret_cast<const uint4*>(scratch + r * kRowBytes + ((c ^ (r & (kChunks - 1))) << 4));
+    if (row0 + r < M)
+      *reinterpret_cast<uint4*>(out + static_cast<int64_t>(row0 + r) * out_row_bytes + c * 16) = val;
+  }
+}
+
 template <bool SILU, bool LORA, bool F32OUT>
-__global__ void __launch_bounds__(kPairThreads, 1) k_fp4gemm_pair(
+__global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_wq,
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_b,
     const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_ws,
     const float* __restrict__ ts_x, const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K,
     int rank, int ldo, uint32_t* __restrict__ status) {
   using C = PairCfg;
+  constexpr int kPairCpWarps = PairRoles<SILU>::kCpWarps;
+  constexpr int kPairEpiWarp0 = PairRoles<SILU>::kEpiWarp0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi_scratch = smem + C::kStages * C::kStageBytes;
@@ -365,8 +403,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_fp4gemm_pair(
   uint64_t* tmem_full = sf_full + C::kStages;
   uint64_t* tmem_empty = tmem_full + 1;
   uint64_t* drain_bar = tmem_empty + 1;
-  uint64_t* drain_cp = drain_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_cp + 1);
+  uint64_t* drain_cp = drain_bar + 1;   // one per copy warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_cp + kPairCpWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -376,12 +414,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_fp4gemm_pair(
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_full[s], 1);
+      mbar_init(&sf_full[s], kPairCpWarps);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, 2 * C::kEpiWarps);
     mbar_init(drain_bar, 1);
-    mbar_init(drain_cp, 1);
+    for (int w = 0; w < kPairCpWarps; ++w) mbar_init(&drain_cp[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_xq);
@@ -490,8 +528,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_fp4gemm_pair(
       tc_commit_pair(drain_bar);
       mbar_drain(drain_bar, 0);
     }
-  } else if (warp == 2) {
+  } else if (warp < kPairEpiWarp0) {
     // ------------------------------------------------- scale atoms -> TMEM
+    // Copy i (0..11) of a stage: K step j = i / 3; kind i % 3 = A rows, B half 0, B half 1.
+    const int cw = warp - 2;
     if (lane == 0 && leader) {
       int st = 0;
       uint32_t ph = 0;
@@ -501,12 +541,15 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_fp4gemm_pair(
           tc_fence_after();
           const int nsub = min(4, (K - kc * 256) >> 6);
           const uint32_t sfa_addr = smem_u32(smem + st * C::kStageBytes) + C::kABytes + C::kBBytes;
-          const uint32_t sfb_addr = sfa_addr + C::kSfaBytes;
           const uint32_t sf_col = tmem + 256 + st * C::kSfCols;
-          for (int j = 0; j < nsub; ++j) {
-            tmem_cp_sf_atom_pair(sf_col + 4 * j, sdesc_sf_atom(sfa_addr + j * 512));
-            tmem_cp_sf_atom_pair(sf_col + 16 + 8 * j, sdesc_sf_atom(sfb_addr + j * 512));
-            tmem_cp_sf_atom_pair(sf_col + 16 + 8 * j + 4, sdesc_sf_atom(sfb_addr + 2048 + j * 512));
+          for (int i = cw; i < 12; i += kPairCpWarps) {
+            const int j = i / 3, kind = i - 3 * j;
+            if (j >= nsub) continue;
+            if (kind == 0)
+              tmem_cp_sf_atom_pair(sf_col + 4 * j, sdesc_sf_atom(sfa_addr + j * 512));
+            else
+              tmem_cp_sf_atom_pair(sf_col + 16 + 8 * j + 4 * (kind - 1),
+                                   sdesc_sf_atom(sfa_addr + C::kSfaBytes + (kind - 1) * 2048 + j * 512));
           }
           tc_commit_pair(&sf_full[st]);
           if (++st == C::kStages) { st = 0; ph ^= 1; }
@@ -518,21 +561,23 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_fp4gemm_pair(
         }
       }
     cp_done:
-      tc_commit_pair(drain_cp);
-      mbar_drain(drain_cp, 0);
+      tc_commit_pair(&drain_cp[cw]);
+      mbar_drain(&drain_cp[cw], 0);
     }
-  } else if (warp < 3 + C::kEpiWarps) {
+  } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quarter of this warp
-    const int e = warp - 3;
+    const int e = warp - kPairEpiWarp0;
     const int half = e >> 2;                 // which half of the tile's columns
     uint8_t* scratch = epi_scratch + e * C::kEpiScratch;
     const float scale = __fmul_rn(*ts_x, *ts_w);
     const uint32_t leader_tmem_empty = cluster_addr(tmem_empty, 0);
     constexpr int kEsize = F32OUT ? 4 : 2;
-    constexpr int kColsPerPass = 128 / kEsize;            // 128-byte row segment per pass
-    constexpr int kOutCols = SILU ? 64 : 128;             // output columns of this warp
-    constexpr int kPasses = kOutCols / kColsPerPass;
+    // bf16: one round of 128 (64 with SiLU) output columns; fp32: rounds of 64 (SiLU: one of 64)
+    constexpr int kRoundCols = (F32OUT && !SILU) ? 64 : (SILU ? 64 : 128);
+    constexpr int kRounds = (SILU ? 64 : 128) / kRoundCols;
+    constexpr int kRowBytes = kRoundCols * kEsize;       // 128 or 256
+    constexpr int kChunks = kRowBytes / 16;
     uint32_t acc_ph = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
       int tm, tn;
@@ -540,77 +585,85 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_fp4gemm_pair(
       if (!mbar_wait(tmem_full, acc_ph, ab)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-      uint32_t v[4][32];
-      if (SILU) {
-        tmem_ld32(taddr + half * 64, v[0]);
-        tmem_ld32(taddr + half * 64 + 32, v[1]);
-        tmem_ld32(taddr + 128 + half * 64, v[2]);
-        tmem_ld32(taddr + 128 + half * 64 + 32, v[3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tmem_ld32(taddr + half * 128 + 32 * i, v[i]);
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
-      acc_ph ^= 1;
-
       const int row0 = tm * 256 + 128 * static_cast<int>(crank) + 32 * q;   // first row of this warp
       const int col0 = SILU ? tn * 128 + half * 64 : tn * 256 + half * 128;
-      const int64_t row_bytes = static_cast<int64_t>(ldo) * kEsize;
+      const int64_t out_row_bytes = static_cast<int64_t>(ldo) * kEsize;
+      if (SILU) {
+        // all 64 gate and 64 up columns of this warp in registers, release the accumulator, then SiLU*up
+        uint32_t g0[32], g1[32], u0[32], u1[32];
+        tmem_ld32(taddr + half * 64, g0);
+        tmem_ld32(taddr + half * 64 + 32, g1);
+        tmem_ld32(taddr + 128 + half * 64, u0);
+        tmem_ld32(taddr + 128 + half * 64 + 32, u1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
 #pragma unroll
-      for (int p = 0; p < kPasses; ++p) {
-        // this thread's row segment (128 bytes) -> swizzled scratch row `lane`, 16 bytes at a time
+        for (int c32 = 0; c32 < 2; ++c32) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
+          for (int q4 = 0; q4 < 32 * kEsize / 16; ++q4) {
+            uint32_t w[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (F32OUT) {
-              const int col = p * 32 + 4 * c + i;
-              float h;
-              if (SILU) {
-                const float g = __fmul_rn(scale, __uint_as_float(v[col >> 5][col & 31]));
-                const float u = __fmul_rn(scale, __uint_as_float(v[2 + (col >> 5)][col & 31]));
-                h = __fmul_rn(silu(g), u);
+            for (int i = 0; i < 4; ++i) {
+              if (F32OUT) {
+                const int k = 4 * q4 + i;
+                w[i] = __float_as_uint(silu_mul_fast(scale, c32 ? g1[k] : g0[k], c32 ? u1[k] : u0[k]));
               } else {
-                h = __fmul_rn(scale, __uint_as_float(v[col >> 5][col & 31]));
+                const int k = 8 * q4 + 2 * i;
+                w[i] = pack_bf16x2(silu_mul_fast(scale, c32 ? g1[k] : g0[k], c32 ? u1[k] : u0[k]),
+                                   silu_mul_fast(scale, c32 ? g1[k + 1] : g0[k + 1], c32 ? u1[k + 1] : u0[k + 1]));
               }
-              w[i] = __float_as_uint(h);
-            } else {
-              float h2[2];
-#pragma unroll
-              for (int k2 = 0; k2 < 2; ++k2) {
-                const int col = p * 64 + 8 * c + 2 * i + k2;
-                if (SILU) {
-                  const float g = __fmul_rn(scale, __uint_as_float(v[col >> 5][col & 31]));
-                  const float u = __fmul_rn(scale, __uint_as_float(v[2 + (col >> 5)][col & 31]));
-                  h2[k2] = __fmul_rn(silu(g), u);
-                } else {
-                  h2[k2] = __fmul_rn(scale, __uint_as_float(v[col >> 5][col & 31]));
-                }
-              }
-              w[i] = pack_bf16x2(h2[0], h2[1]);
             }
+            const int chunk = c32 * (32 * kEsize / 16) + q4;
+            *reinterpret_cast<uint4*>(scratch + lane * kRowBytes + ((chunk ^ (lane & (kChunks - 1))) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
-          *reinterpret_cast<uint4*>(scratch + lane * 128 + ((c ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         __syncwarp();
-        // 4 rows x 128 contiguous bytes per store instruction
+        epi_flush<kRowBytes>(scratch, static_cast<uint8_t*>(out) + static_cast<int64_t>(col0) * kEsize, out_row_bytes,
+                             row0, M, lane);
+        __syncwarp();
+      } else {
+#pragma unroll 1
+      for (int rd = 0; rd < kRounds; ++rd) {
+        // drain this round's columns 32 at a time into the scratch row of this lane
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int r = it * 4 + (lane >> 3);
-          const int c = lane & 7;
-          const uint4 val = *reinterpret_cast<const uint4*>(scratch + r * 128 + ((c ^ (r & 7)) << 4));
-          if (row0 + r < M) {
-            uint8_t* dst = static_cast<uint8_t*>(out) + static_cast<int64_t>(row0 + r) * row_bytes +
-                           static_cast<int64_t>(col0 + p * kColsPerPass) * kEsize + c * 16;
-            *reinterpret_cast<uint4*>(dst) = val;
+        for (int c32 = 0; c32 < kRoundCols / 32; ++c32) {
+          const int col = rd * kRoundCols + c32 * 32;            // column inside this warp's range
+          uint32_t a[32];
+          tmem_ld32(taddr + half * 128 + col, a);
+          tmem_ld_wait();
+          // 32 values -> 64 bytes (bf16) or 128 bytes (fp32) at byte c32 * (32 * esize) of the row
+#pragma unroll
+          for (int q4 = 0; q4 < 32 * kEsize / 16; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (F32OUT) {
+                w[i] = __float_as_uint(__fmul_rn(scale, __uint_as_float(a[4 * q4 + i])));
+              } else {
+                const int k = 8 * q4 + 2 * i;
+                w[i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a[k])), __fmul_rn(scale, __uint_as_float(a[k + 1])));
+              }
+            }
+            const int chunk = c32 * (32 * kEsize / 16) + q4;
+            *reinterpret_cast<uint4*>(scratch + lane * kRowBytes + ((chunk ^ (lane & (kChunks - 1))) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
+        if (rd == kRounds - 1) {   // every accumulator column of this warp has been read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+        }
+        __syncwarp();
+        epi_flush<kRowBytes>(scratch, static_cast<uint8_t*>(out) + static_cast<int64_t>(col0 + rd * kRoundCols) * kEsize,
+                             out_row_bytes, row0, M, lane);
         __syncwarp();
       }
+      }
+      acc_ph ^= 1;
     }
   }
   tc_fence_before();
@@ -634,7 +687,7 @@ static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStre
   const int grid = 2 * (tiles < max_pairs ? tiles : max_pairs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kPairThreads);
+  cfg.blockDim = dim3(PairRoles<SILU>::kThreads);
   cfg.dynamicSmemBytes = PairCfg::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
