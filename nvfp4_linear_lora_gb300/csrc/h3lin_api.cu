@@ -146,7 +146,7 @@ h3lin_status quantize_impl(const void* x, int64_t M, int64_t K, const float* pqs
   const RowPlan plan = plan_rows(M, K, d.sm_count);
   if (launch_amax(x, int(M), int(K), pqs, partials, plan, stream) != cudaSuccess) return H3LIN_E_CUDA;
   if (launch_quant(x, int(M), int(K), pqs, partials, plan.blocks, codes, scales, ts, plan, nullptr, nullptr, 0,
-                   0.0f, nullptr, stream) != cudaSuccess)
+                   0.0f, nullptr, d.sm_count, stream) != cudaSuccess)
     return H3LIN_E_CUDA;
   return H3LIN_OK;
 }
@@ -239,7 +239,7 @@ h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
   const float lora_k = c.lora ? c.strength * (c.adapter->alpha / float(c.rank)) : 0.0f;
   if (launch_quant(c.x, int(c.M), int(c.K), c.pqs, partials, nparts, xq, xs, ts_x, plan,
                    c.lora ? c.adapter->B : nullptr, c.lora ? bp : nullptr, c.lora ? c.N * c.rank : 0, lora_k,
-                   c.w->tensor_scale, stream) != cudaSuccess)
+                   c.w->tensor_scale, c.dev.sm_count, stream) != cudaSuccess)
     return H3LIN_E_CUDA;
   return H3LIN_OK;
 }

@@ -27,7 +27,7 @@
 namespace h3lin {
 
 constexpr int kGemmThreads = 320;
-constexpr int kGroupM = 8;
+constexpr int kGroupM = 32;
 
 template <int BN>
 struct GemmCfg {

@@ -35,7 +35,7 @@ cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const fl
                          void* codes, void* scales, float* ts_out, const RowPlan& p,
                          // optional: B' = bf16(B * lora_k / (ts * ts_w)), elems % 8 == 0
                          const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
-                         cudaStream_t st);
+                         int sm_count, cudaStream_t st);
 // amax pass fused with u = A(x) (bf16 [M, rank]); returns grid size in *nparts.
 cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
                              int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,

@@ -97,43 +97,71 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict_
 }
 
 // ---------------------------------------------------------------- k_quant
+// Thread t owns 16-element block b = t % (K/16) of rows r0, r0 + R, ... with
+// r0 = t / (K/16): its 16 per-channel scales stay in registers, the block
+// scale is computed once per block, and the four threads of a 64-column group
+// (never split across rows, K % 64 == 0) assemble the 32-bit scale word.
 struct QuantCtx {
   float ts, six_ts;
-  int M, kc, K;
-  uint32_t* codes;
+  int kb, K;
+  uint2* codes;      // 8 bytes = 16 codes per block
   uint8_t* scales;
 };
 
-// Quantise one 8-element chunk (lanes 2j, 2j+1 of an aligned 8-lane group
-// form 16-element block j of the group's 64 columns).
-__device__ __forceinline__ void quant_chunk(const QuantCtx& q, int row, int c, const uint4& w,
-                                            const float (&s)[8], unsigned gmask, int lane) {
-  float v[8];
-  prescale8(w, s, v);
-  float bm = absmax8(v);
-  bm = fmaxf(bm, __shfl_xor_sync(gmask, bm, 1, 8));
+__device__ __forceinline__ void load_scale16(const float* __restrict__ pqs, int b, float (&s)[16]) {
+  if (pqs == nullptr) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = 1.0f;
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(pqs) + 4 * b;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 a = __ldg(p + i);
+      s[4 * i] = a.x; s[4 * i + 1] = a.y; s[4 * i + 2] = a.z; s[4 * i + 3] = a.w;
+    }
+  }
+}
+
+// Quantise one 16-element block (two 16-byte halves) of row `row`.
+__device__ __forceinline__ void quant_block(const QuantCtx& q, int row, int b, const uint4& w0, const uint4& w1,
+                                            const float (&s)[16], unsigned gmask, int lane) {
+  float v[16];
+  {
+    float h0[8], h1[8], s0[8], s1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { s0[i] = s[i]; s1[i] = s[8 + i]; }
+    prescale8(w0, s0, h0);
+    prescale8(w1, s1, h1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { v[i] = h0[i]; v[8 + i] = h1[i]; }
+  }
+  float bm = fabsf(v[0]);
+#pragma unroll
+  for (int i = 1; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
   const uint32_t sb = e4m3_rn_satfinite(__fdiv_rn(bm, q.six_ts));
   const float d = __fmul_rn(e4m3_to_float(sb), q.ts);
   const float inv = __frcp_rn(d);
-  float qv[8];
+  float qa[8], qb[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) qv[i] = __fmul_rn(v[i], inv);
-  const uint32_t code = isfinite(inv) ? e2m1x8(qv) : 0u;
-  q.codes[static_cast<int64_t>(row) * q.kc + c] = code;
-  const uint32_t s1 = __shfl_down_sync(gmask, sb, 2, 8);
-  const uint32_t s2 = __shfl_down_sync(gmask, sb, 4, 8);
-  const uint32_t s3 = __shfl_down_sync(gmask, sb, 6, 8);
-  if ((lane & 7) == 0) {
-    *reinterpret_cast<uint32_t*>(q.scales + sf_offset(row, (c >> 1), q.K)) =
-        sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  for (int i = 0; i < 8; ++i) {
+    qa[i] = __fmul_rn(v[i], inv);
+    qb[i] = __fmul_rn(v[8 + i], inv);
   }
+  uint2 code = make_uint2(0u, 0u);
+  if (isfinite(inv)) code = make_uint2(e2m1x8(qa), e2m1x8(qb));
+  q.codes[static_cast<int64_t>(row) * q.kb + b] = code;
+  const uint32_t s1 = __shfl_down_sync(gmask, sb, 1, 4);
+  const uint32_t s2 = __shfl_down_sync(gmask, sb, 2, 4);
+  const uint32_t s3 = __shfl_down_sync(gmask, sb, 3, 4);
+  if ((lane & 3) == 0)
+    *reinterpret_cast<uint32_t*>(q.scales + sf_offset(row, b, q.K)) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
 // Rows are visited from the last to the first: the amax pass streamed them
 // in ascending order, so the tail of x is still in L2 when this pass starts.
 __global__ void __launch_bounds__(kQuantThreads) k_quant(
-    const uint4* __restrict__ x, int M, int Mpad, int kc, int K, const float* __restrict__ pqs,
-    const float* __restrict__ partials, int nparts, uint32_t* __restrict__ codes, uint8_t* __restrict__ scales,
+    const uint4* __restrict__ x, int M, int Mpad, int K, const float* __restrict__ pqs,
+    const float* __restrict__ partials, int nparts, uint2* __restrict__ codes, uint8_t* __restrict__ scales,
     float* __restrict__ ts_out, int rows_step, const uint4* __restrict__ b_src, uint4* __restrict__ b_dst,
     int64_t b_chunks, float lora_k, const float* __restrict__ ts_w) {
   __shared__ float red[kQuantThreads / 32];
@@ -143,33 +171,43 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant(
   float ts = __fdiv_rn(amax, 2688.0f);
   if (ts == 0.0f) ts = 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
-  QuantCtx q{ts, __fmul_rn(6.0f, ts), M, kc, K, codes, scales};
+  const int kb = K >> 4;
+  QuantCtx q{ts, __fmul_rn(6.0f, ts), kb, K, codes, scales};
 
   const int tid = blockIdx.x * kQuantThreads + threadIdx.x;
-  const int c = tid % kc;
-  const int r0 = tid / kc;
+  const int b = tid % kb;
+  const int r0 = tid / kb;
   const int lane = threadIdx.x & 31;
-  const unsigned gmask = 0xFFu << (lane & 24);
+  const unsigned gmask = 0xFu << (lane & 28);
+  const int kc = K >> 3;   // 16-byte chunks per row
   if (r0 < rows_step) {
-    float s[8];
-    load_scale8(pqs, c, s);
+    float s[16];
+    load_scale16(pqs, b, s);
     for (int i = r0; i < Mpad; i += 2 * rows_step) {
       const int ra = Mpad - 1 - i;
       const bool has_b = i + rows_step < Mpad;
       const int rb = Mpad - 1 - (i + rows_step);
-      uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
-      if (ra < M) wa = __ldcs(x + static_cast<int64_t>(ra) * kc + c);
-      if (has_b && rb < M) wb = __ldcs(x + static_cast<int64_t>(rb) * kc + c);
+      uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, c0 = a0, c1 = a0;
       if (ra < M) {
-        quant_chunk(q, ra, c, wa, s, gmask, lane);
-      } else if ((lane & 7) == 0) {
-        *reinterpret_cast<uint32_t*>(scales + sf_offset(ra, (c >> 1), K)) = 0u;
+        const uint4* p = x + static_cast<int64_t>(ra) * kc + 2 * b;
+        a0 = __ldcs(p);
+        a1 = __ldcs(p + 1);
+      }
+      if (has_b && rb < M) {
+        const uint4* p = x + static_cast<int64_t>(rb) * kc + 2 * b;
+        c0 = __ldcs(p);
+        c1 = __ldcs(p + 1);
+      }
+      if (ra < M) {
+        quant_block(q, ra, b, a0, a1, s, gmask, lane);
+      } else if ((lane & 3) == 0) {
+        *reinterpret_cast<uint32_t*>(scales + sf_offset(ra, b, K)) = 0u;
       }
       if (has_b) {
         if (rb < M) {
-          quant_chunk(q, rb, c, wb, s, gmask, lane);
-        } else if ((lane & 7) == 0) {
-          *reinterpret_cast<uint32_t*>(scales + sf_offset(rb, (c >> 1), K)) = 0u;
+          quant_block(q, rb, b, c0, c1, s, gmask, lane);
+        } else if ((lane & 3) == 0) {
+          *reinterpret_cast<uint32_t*>(scales + sf_offset(rb, b, K)) = 0u;
         }
       }
     }
@@ -390,12 +428,36 @@ cudaError_t launch_amax(const void* x, int M, int K, const float* pqs, float* pa
   return cudaGetLastError();
 }
 
+// One wave of k_quant: as many 256-thread blocks as fit on the device at once;
+// each thread owns one 16-element block column of K / 16.
+static RowPlan plan_quant(int64_t M, int64_t K, int sm_count) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant, kQuantThreads, 0) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 4;
+    }
+    per_sm = n;
+  }
+  const int64_t kb = K / 16;
+  const int64_t threads = static_cast<int64_t>(sm_count) * per_sm * kQuantThreads;
+  int64_t rows_step = threads / kb;
+  if (rows_step < 1) rows_step = 1;
+  const int64_t mpad = ((M + 127) / 128) * 128;
+  if (rows_step > mpad) rows_step = mpad;
+  const int64_t blocks = (kb * rows_step + kQuantThreads - 1) / kQuantThreads;
+  return RowPlan{static_cast<int>(blocks), static_cast<int>(rows_step)};
+}
+
 cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
-                         void* codes, void* scales, float* ts_out, const RowPlan& p, const void* b_src,
-                         void* b_dst, int64_t b_elems, float lora_k, const float* ts_w, cudaStream_t st) {
+                         void* codes, void* scales, float* ts_out, const RowPlan& /*amax plan*/, const void* b_src,
+                         void* b_dst, int64_t b_elems, float lora_k, const float* ts_w, int sm_count,
+                         cudaStream_t st) {
   const int Mpad = ((M + 127) / 128) * 128;
+  const RowPlan p = plan_quant(M, K, sm_count);
   k_quant<<<p.blocks, kQuantThreads, 0, st>>>(
-      static_cast<const uint4*>(x), M, Mpad, K / 8, K, pqs, partials, nparts, static_cast<uint32_t*>(codes),
+      static_cast<const uint4*>(x), M, Mpad, K, pqs, partials, nparts, static_cast<uint2*>(codes),
       static_cast<uint8_t*>(scales), ts_out, p.rows_step, static_cast<const uint4*>(b_src),
       static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w);
   return cudaGetLastError();
