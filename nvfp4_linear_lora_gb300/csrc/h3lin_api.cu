@@ -92,6 +92,22 @@ bool make_sf_map(CUtensorMap* m, const void* base, uint64_t bytes) {
   return r == CUDA_SUCCESS;
 }
 
+// Output [rows, cols] (bf16 or fp32) stored by 32-row x 128-byte boxes,
+// 128-byte swizzle (the epilogue's staging layout).
+bool make_out_map(CUtensorMap* m, void* base, bool f32, int64_t cols, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t esize = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {uint64_t(cols), uint64_t(rows)};
+  cuuint64_t strides[1] = {uint64_t(cols) * esize};
+  cuuint32_t box[2] = {uint32_t(128 / esize), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major 2-D tensor [rows, inner] with a 128-byte-swizzled box.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
@@ -278,7 +294,8 @@ h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream) {
   // CTA-pair kernel for N % 256 == 0 (and SiLU*up, whose N is a multiple of 256)
   g.pair = (c.N % 256 == 0) && c.dev.sm_count >= 2 &&
            make_sf_map(&g.tm_xs, g.xs, size_t((c.M + 127) / 128 * 128) * size_t(c.K / 16)) &&
-           make_sf_map(&g.tm_ws, g.ws, size_t(c.N) * size_t(c.K / 16));
+           make_sf_map(&g.tm_ws, g.ws, size_t(c.N) * size_t(c.K / 16)) &&
+           make_out_map(&g.tm_out, c.out, c.f32out, g.ldo, c.M);
   if (launch_fp4gemm(g, c.dev.sm_count, stream) != cudaSuccess) return H3LIN_E_CUDA;
   return H3LIN_OK;
 }

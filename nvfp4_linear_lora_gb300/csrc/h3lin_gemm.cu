@@ -332,9 +332,11 @@ static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t 
 //                 a copy costs its issuing thread a long issue slot, so six
 //                 issuing warps keep the twelve copies of a stage off the
 //                 critical path (they overlap the previous stage's MMAs)
-//   warps 8-15    epilogue: drain TMEM 32 columns at a time into a per-warp
-//                 shared scratch (already scaled / SiLU*up / packed), release
-//                 the accumulator, then store whole 128-byte lines
+//   warps 8-15    epilogue: drain TMEM 32 columns at a time, convert (scale,
+//                 SiLU*up, bf16/fp32), stage 32 rows x 128 bytes in a per-warp
+//                 shared scratch and store whole 128-byte lines; the
+//                 accumulator is released as soon as its last columns are in
+//                 registers
 // Copy warps: six for plain tiles; four for SiLU*up tiles, whose epilogue
 // keeps all 128 accumulator columns in registers (more registers per thread).
 template <bool SILU> struct PairRoles {
@@ -348,10 +350,10 @@ struct PairCfg {
   static constexpr int kSfaBytes = 4 * 512;
   static constexpr int kSfbBytes = 2 * 4 * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;   // 38 KB
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 5;
   static constexpr int kSfCols = 16 + 32;
   static constexpr int kEpiWarps = 8;
-  static constexpr int kEpiScratch = 8192;                                          // 32 rows x 256 bytes
+  static constexpr int kEpiScratch = 4096;                                          // 32 rows x 128 bytes
   static constexpr int kSmem = kStages * kStageBytes + kEpiWarps * kEpiScratch + 1024 + 256;
   static constexpr int kTmemCols = 512;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -367,21 +369,22 @@ __device__ __forceinline__ float silu_mul_fast(float scale, uint32_t acc_g, uint
   return __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
 }
 
-// Store the warp's scratch (32 rows x `row_bytes` bytes, 16-byte chunks swizzled
-// by row) to global rows row0.. with whole-line stores; rows >= M skipped.
-template <int kRowBytes>
-__device__ __forceinline__ void epi_flush(const uint8_t* scratch, uint8_t* out, int64_t out_row_bytes, int row0,
-                                          int M, int lane) {
-  constexpr int kChunks = kRowBytes / 16;          // 16-byte chunks per row
-  constexpr int kRowsPerStep = 32 / kChunks;       // rows written by one warp-wide store
-#pragma unroll
-  for (int it = 0; it < 32 / kRowsPerStep; ++it) {
-    const int r = it * kRowsPerStep + lane / kChunks;
-    const int c = lane % kChunks;
-    const uint4 val = *reinterpret_cast<const uint4*>(scratch + r * kRowBytes + ((c ^ (r & (kChunks - 1))) << 4));
-    if (row0 + r < M)
-      *reinterpret_cast<uint4*>(out + static_cast<int64_t>(row0 + r) * out_row_bytes + c * 16) = val;
+// The warp's scratch block (32 rows x 128 bytes, 16-byte chunks swizzled by
+// row exactly as the 128-byte TMA swizzle lays them out) -> global through the
+// TMA engine; rows >= M are clipped by the tensor map.
+__device__ __forceinline__ void epi_store(const CUtensorMap* tm_out, const uint8_t* scratch, int col, int row0,
+                                          int lane) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm_out, scratch, col, row0);
+    bulk_commit_group();
   }
+}
+// Before rewriting the scratch: the previous TMA store has finished reading it.
+__device__ __forceinline__ void epi_scratch_ready(int lane) {
+  if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
 }
 
 template <bool SILU, bool LORA, bool F32OUT>
@@ -389,6 +392,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_wq,
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_b,
     const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_ws,
+    const __grid_constant__ CUtensorMap tm_out,
     const float* __restrict__ ts_x, const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K,
     int rank, int ldo, uint32_t* __restrict__ status) {
   using C = PairCfg;
@@ -573,11 +577,10 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     const float scale = __fmul_rn(*ts_x, *ts_w);
     const uint32_t leader_tmem_empty = cluster_addr(tmem_empty, 0);
     constexpr int kEsize = F32OUT ? 4 : 2;
-    // bf16: one round of 128 (64 with SiLU) output columns; fp32: rounds of 64 (SiLU: one of 64)
-    constexpr int kRoundCols = (F32OUT && !SILU) ? 64 : (SILU ? 64 : 128);
+    // rounds of 128-byte row segments: 64 bf16 or 32 fp32 output columns each
+    constexpr int kRoundCols = 128 / kEsize;
     constexpr int kRounds = (SILU ? 64 : 128) / kRoundCols;
-    constexpr int kRowBytes = kRoundCols * kEsize;       // 128 or 256
-    constexpr int kChunks = kRowBytes / 16;
+    static_assert(kRoundCols * kEsize == 128, "128-byte scratch rows");
     uint32_t acc_ph = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
       int tm, tn;
@@ -587,7 +590,6 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
       const int row0 = tm * 256 + 128 * static_cast<int>(crank) + 32 * q;   // first row of this warp
       const int col0 = SILU ? tn * 128 + half * 64 : tn * 256 + half * 128;
-      const int64_t out_row_bytes = static_cast<int64_t>(ldo) * kEsize;
       if (SILU) {
         // all 64 gate and 64 up columns of this warp in registers, release the accumulator, then SiLU*up
         uint32_t g0[32], g1[32], u0[32], u1[32];
@@ -599,72 +601,97 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+        // 64 output columns: one 128-byte round (bf16) or two (fp32)
 #pragma unroll
-        for (int c32 = 0; c32 < 2; ++c32) {
+        for (int sr = 0; sr < kRounds; ++sr) {
+          epi_scratch_ready(lane);
 #pragma unroll
-          for (int q4 = 0; q4 < 32 * kEsize / 16; ++q4) {
+          for (int q4 = 0; q4 < 8; ++q4) {
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               if (F32OUT) {
-                const int k = 4 * q4 + i;
-                w[i] = __float_as_uint(silu_mul_fast(scale, c32 ? g1[k] : g0[k], c32 ? u1[k] : u0[k]));
+                const int k = 4 * q4 + i;   // column 32 * sr + k
+                w[i] = __float_as_uint(silu_mul_fast(scale, sr ? g1[k] : g0[k], sr ? u1[k] : u0[k]));
               } else {
-                const int k = 8 * q4 + 2 * i;
-                w[i] = pack_bf16x2(silu_mul_fast(scale, c32 ? g1[k] : g0[k], c32 ? u1[k] : u0[k]),
-                                   silu_mul_fast(scale, c32 ? g1[k + 1] : g0[k + 1], c32 ? u1[k + 1] : u0[k + 1]));
+                const int col = 8 * q4 + 2 * i;
+                const uint32_t ga = col < 32 ? g0[col] : g1[col - 32], ua = col < 32 ? u0[col] : u1[col - 32];
+                const uint32_t gb = col < 32 ? g0[col + 1] : g1[col - 31], ub = col < 32 ? u0[col + 1] : u1[col - 31];
+                w[i] = pack_bf16x2(silu_mul_fast(scale, ga, ua), silu_mul_fast(scale, gb, ub));
               }
             }
-            const int chunk = c32 * (32 * kEsize / 16) + q4;
-            *reinterpret_cast<uint4*>(scratch + lane * kRowBytes + ((chunk ^ (lane & (kChunks - 1))) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(scratch + lane * 128 + ((q4 ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
+          epi_store(&tm_out, scratch, col0 + sr * kRoundCols, row0, lane);
         }
-        __syncwarp();
-        epi_flush<kRowBytes>(scratch, static_cast<uint8_t*>(out) + static_cast<int64_t>(col0) * kEsize, out_row_bytes,
-                             row0, M, lane);
-        __syncwarp();
-      } else {
-#pragma unroll 1
-      for (int rd = 0; rd < kRounds; ++rd) {
-        // drain this round's columns 32 at a time into the scratch row of this lane
-#pragma unroll
-        for (int c32 = 0; c32 < kRoundCols / 32; ++c32) {
-          const int col = rd * kRoundCols + c32 * 32;            // column inside this warp's range
-          uint32_t a[32];
-          tmem_ld32(taddr + half * 128 + col, a);
+      } else if (!F32OUT) {
+        // bf16: pack all 128 columns of this warp into 64 registers, release the
+        // accumulator, then stage and store two 64-column rounds
+        // two loads in flight per wait: columns 0-63, then 64-127 (released right after)
+        uint32_t w[64];
+        {
+          uint32_t a0[32], a1[32];
+          tmem_ld32(taddr + half * 128, a0);
+          tmem_ld32(taddr + half * 128 + 32, a1);
           tmem_ld_wait();
-          // 32 values -> 64 bytes (bf16) or 128 bytes (fp32) at byte c32 * (32 * esize) of the row
 #pragma unroll
-          for (int q4 = 0; q4 < 32 * kEsize / 16; ++q4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (F32OUT) {
-                w[i] = __float_as_uint(__fmul_rn(scale, __uint_as_float(a[4 * q4 + i])));
-              } else {
-                const int k = 8 * q4 + 2 * i;
-                w[i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a[k])), __fmul_rn(scale, __uint_as_float(a[k + 1])));
-              }
-            }
-            const int chunk = c32 * (32 * kEsize / 16) + q4;
-            *reinterpret_cast<uint4*>(scratch + lane * kRowBytes + ((chunk ^ (lane & (kChunks - 1))) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a0[2 * i])), __fmul_rn(scale, __uint_as_float(a0[2 * i + 1])));
+            w[16 + i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a1[2 * i])), __fmul_rn(scale, __uint_as_float(a1[2 * i + 1])));
           }
         }
-        if (rd == kRounds - 1) {   // every accumulator column of this warp has been read
+        {
+          uint32_t a2[32], a3[32];
+          tmem_ld32(taddr + half * 128 + 64, a2);
+          tmem_ld32(taddr + half * 128 + 96, a3);
+          tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[32 + i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a2[2 * i])), __fmul_rn(scale, __uint_as_float(a2[2 * i + 1])));
+            w[48 + i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a3[2 * i])), __fmul_rn(scale, __uint_as_float(a3[2 * i + 1])));
+          }
+        }
+#pragma unroll
+        for (int rd = 0; rd < 2; ++rd) {
+          epi_scratch_ready(lane);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(scratch + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(w[rd * 32 + 4 * c], w[rd * 32 + 4 * c + 1], w[rd * 32 + 4 * c + 2], w[rd * 32 + 4 * c + 3]);
+          epi_store(&tm_out, scratch, col0 + rd * 64, row0, lane);
+        }
+      } else {
+        // fp32 (checking mode): rounds of 32 columns; the accumulator is released
+        // after the last round's columns are in registers
+        uint32_t w[32];
+#pragma unroll 1
+        for (int rd = 0; rd < kRounds; ++rd) {
+          uint32_t a[32];
+          tmem_ld32(taddr + half * 128 + rd * 32, a);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__fmul_rn(scale, __uint_as_float(a[i])));
+          if (rd == kRounds - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+          }
+          epi_scratch_ready(lane);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(scratch + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          epi_store(&tm_out, scratch, col0 + rd * 32, row0, lane);
         }
         __syncwarp();
-        epi_flush<kRowBytes>(scratch, static_cast<uint8_t*>(out) + static_cast<int64_t>(col0 + rd * kRoundCols) * kEsize,
-                             out_row_bytes, row0, M, lane);
-        __syncwarp();
-      }
       }
       acc_ph ^= 1;
     }
+    if (lane == 0) bulk_wait_group0();   // this warp's output stores are complete
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -697,8 +724,8 @@ static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStre
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.tm_xs, a.tm_ws, a.ts_x, a.ts_w, a.out,
-                            a.M, a.N, a.K, a.rank, a.ldo, a.status);
+  return cudaLaunchKernelEx(&cfg, kern, a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.tm_xs, a.tm_ws, a.tm_out, a.ts_x, a.ts_w,
+                            a.out, a.M, a.N, a.K, a.rank, a.ldo, a.status);
 }
 
 template <bool F32OUT>

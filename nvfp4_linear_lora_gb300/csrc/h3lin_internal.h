@@ -44,6 +44,7 @@ cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, i
 struct GemmArgs {
   CUtensorMap tm_xq, tm_wq, tm_u, tm_b;
   CUtensorMap tm_xs, tm_ws;   // scale bytes viewed as [bytes / 256, 256] (pair kernel)
+  CUtensorMap tm_out;         // output [M, ldo], 32-row x 128-byte boxes (pair kernel)
   const uint8_t* xs;
   const uint8_t* ws;
   const float* ts_x;
