@@ -236,15 +236,36 @@ def pack_all(host):
 
 
 def calibrate_sample(host, packed, seconds):
-    """Pick (rows, cols) so that one oracle sample run takes about ``seconds``."""
+    """Pick (rows, cols) so that one oracle sample run takes about ``seconds``:
+    widen the column sample first (up to 4096 output columns), then the rows."""
+    S = max(p["x"].shape[0] for p in host if p["x"] is not None)
     m, n = 16, 256
-    t, _ = oracle_sample_run(host, m, n, packed=packed)
-    scale = max(0.25, min(64.0, seconds / max(t, 1e-3)))
-    n = int(max(128, min(8192, n * scale)) // 128 * 128)
+    for _ in range(16):
+        t, _ = oracle_sample_run(host, m, n, packed=packed)
+        if t >= 0.6 * seconds:
+            break
+        grow = min(4.0, seconds / max(t, 1e-3))
+        if n < 4096:
+            n = int(min(4096, n * grow)) // 128 * 128
+        elif m < S:
+            m = int(min(S, m * grow))
+        else:
+            break
     return m, n
 
 
 def cpu_info():
+    """Threads the oracle's BLAS calls use (all host cores unless limited)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((d.get("num_threads") or 0) for d in threadpool_info() if d.get("user_api") == "blas")
+        if n:
+            return n
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
     return os.cpu_count() or 1
 
 
@@ -388,7 +409,7 @@ def native_arm(a, rank, world, local_rank):
             "vs_baseline": None, "dtype": "e2m1+bf16", "data": "synthetic",
             "config": {"workload": f"dit_block_4proj_S{S}", "S": S, "hidden": configs.HIDDEN, "mlp": configs.MLP,
                        "ranks": [p[3] for p in configs.BLOCK_PROJECTIONS], "strength": 1.0,
-                       "l2": "inputs larger than L2 (each activation >= 386 MB), no flush"},
+                       "l2": f"inputs larger than L2 (each activation >= {S * configs.HIDDEN * 2 / 1e6:.0f} MB), no flush"},
             "ms_per_block": ms, "frac_of_fp4_peak": value / world / peak_fp4,
             "flops_per_block": {"total": total, "base_fp4": base, "lora_down": ldown, "lora_up": lup},
             "kernel_ms": {"gemm": gemm_total_ms, "prepare": ms - gemm_total_ms},

@@ -173,6 +173,19 @@ h3lin_status h3lin_forward_gemm(int64_t M, const h3lin_weight* weight, int32_t e
                                 const h3lin_adapter* adapter, float strength, void* out, int32_t out_dtype,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------- failure self-test */
+/* Exercises the kernels' failure path on the device without any fault: a
+ * kernel waits, with a bound of `wait_cycles` SM clock cycles (1 .. 2^31), on
+ * an mbarrier that nothing ever arrives on.  The wait runs out, the kernel
+ * records H3LIN_E_TIMEOUT in the workspace status word (read it with
+ * h3lin_read_status, clear it with h3lin_workspace_init), stops its other
+ * waiter through the CTA abort flag and returns; the context stays usable.
+ * Every wait in the production kernels is bounded the same way (about 2^31
+ * cycles).  No counterpart in the paper: part of the library's failure
+ * detection. */
+h3lin_status h3lin_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t wait_cycles,
+                                         cudaStream_t stream);
+
 /* ----------------------------------------------- forward without allocation */
 /* No counterpart in the paper: a library-level addition.
  *

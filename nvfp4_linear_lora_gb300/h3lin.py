@@ -66,6 +66,7 @@ _SIGNATURES = {
     "h3lin_forward_gemm": (_i32, [_i64, ctypes.POINTER(h3lin_weight), _i32, ctypes.POINTER(h3lin_adapter), _f32,
                                   _vp, _i32, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+    "h3lin_selftest_wait_timeout": (_i32, [_vp, _sz, _i64, _vp]),
     "h3lin_forward_noalloc": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), _i32,
                                      ctypes.POINTER(h3lin_adapter), _f32, _vp, _i32, _vp]),
 }
@@ -149,6 +150,10 @@ def h3lin_forward_noalloc(x, M, pqs, weight, epilogue, adapter, strength, out, o
     wp = ctypes.byref(weight) if weight is not None else None
     ap = ctypes.byref(adapter) if adapter is not None else None
     return lib().h3lin_forward_noalloc(x, M, pqs, wp, epilogue, ap, strength, out, out_dtype, stream)
+
+
+def h3lin_selftest_wait_timeout(ws, ws_bytes, wait_cycles, stream):
+    return lib().h3lin_selftest_wait_timeout(ws, ws_bytes, wait_cycles, stream)
 
 
 def h3lin_read_status(ws, stream):
