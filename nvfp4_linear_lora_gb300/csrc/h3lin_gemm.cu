@@ -493,35 +493,48 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // A tcgen05.mma is accepted only about when the previous one starts, so every
+    // instruction between two MMAs idles the tensor pipe: the loop waits on one
+    // barrier per stage (sf_full: the copy warps commit it only after they saw
+    // the stage's TMA data land, so it implies full) and issues the stage's MMAs
+    // back to back from precomputed descriptors.
     if (lane == 0 && leader) {
       int st = 0;
       uint32_t ph = 0, acc_ph = 0;
       const uint32_t idesc_f4 = idesc_nvfp4_m256(256);
       const uint32_t idesc_bf = idesc_bf16_m256(256);
+      const uint32_t smem0 = smem_u32(smem);
+      const bool k_full = (K & 255) == 0;
       for (int t = pair; t < num_tiles; t += npairs) {
         if (!mbar_wait(tmem_empty, acc_ph ^ 1, ab)) goto mma_done;
         tc_fence_after();
         for (int kc = 0; kc < nk; ++kc) {
-          if (!mbar_wait(&full[st], ph, ab) || !mbar_wait(&sf_full[st], ph, ab)) goto mma_done;
+          if (!mbar_wait(&sf_full[st], ph, ab)) goto mma_done;
           tc_fence_after();
-          const int nsub = min(4, (K - kc * 256) >> 6);
-          const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
-          const uint32_t b_addr = a_addr + C::kABytes;
-          const uint32_t sf_col = tmem + 256 + st * C::kSfCols;
-          for (int j = 0; j < nsub; ++j)
-            mma_nvfp4_pair(tmem, sdesc_kmajor_sw128(a_addr + j * 32), sdesc_kmajor_sw128(b_addr + j * 32), idesc_f4,
-                           sf_col + 4 * j, sf_col + 16 + 8 * j, (kc | j) != 0);
+          const uint32_t a_addr = smem0 + st * C::kStageBytes;
+          // +32 bytes along K = +2 in a descriptor's start-address field
+          const uint64_t ad = sdesc_kmajor_sw128(a_addr), bd = sdesc_kmajor_sw128(a_addr + C::kABytes);
+          const uint32_t sf = tmem + 256 + st * C::kSfCols;
+          if (k_full) {
+            mma_nvfp4_pair(tmem, ad, bd, idesc_f4, sf, sf + 16, kc != 0);
+            mma_nvfp4_pair(tmem, ad + 2, bd + 2, idesc_f4, sf + 4, sf + 24, 1u);
+            mma_nvfp4_pair(tmem, ad + 4, bd + 4, idesc_f4, sf + 8, sf + 32, 1u);
+            mma_nvfp4_pair(tmem, ad + 6, bd + 6, idesc_f4, sf + 12, sf + 40, 1u);
+          } else {
+            const int nsub = min(4, (K - kc * 256) >> 6);
+            for (int j = 0; j < nsub; ++j)
+              mma_nvfp4_pair(tmem, ad + 2 * j, bd + 2 * j, idesc_f4, sf + 4 * j, sf + 16 + 8 * j, (kc | j) != 0);
+          }
           tc_commit_pair_mc(&empty[st]);
           if (++st == C::kStages) { st = 0; ph ^= 1; }
         }
         for (int rc = 0; rc < nr; ++rc) {
-          if (!mbar_wait(&full[st], ph, ab) || !mbar_wait(&sf_full[st], ph, ab)) goto mma_done;
+          if (!mbar_wait(&sf_full[st], ph, ab)) goto mma_done;
           tc_fence_after();
+          const uint32_t a_addr = smem0 + st * C::kStageBytes;
+          const uint64_t ad = sdesc_kmajor_sw128(a_addr), bd = sdesc_kmajor_sw128(a_addr + C::kABytes);
           const int nk16 = min(4, (rank - rc * 64) >> 4);
-          const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
-          const uint32_t b_addr = a_addr + C::kABytes;
-          for (int j = 0; j < nk16; ++j)
-            mma_bf16_pair(tmem, sdesc_kmajor_sw128(a_addr + j * 32), sdesc_kmajor_sw128(b_addr + j * 32), idesc_bf, 1u);
+          for (int j = 0; j < nk16; ++j) mma_bf16_pair(tmem, ad + 2 * j, bd + 2 * j, idesc_bf, 1u);
           tc_commit_pair_mc(&empty[st]);
           if (++st == C::kStages) { st = 0; ph ^= 1; }
         }
