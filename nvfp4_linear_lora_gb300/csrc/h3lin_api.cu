@@ -100,10 +100,10 @@ bool make_out_map(CUtensorMap* m, void* base, bool f32, int64_t cols, int64_t ro
   const uint64_t esize = f32 ? 4 : 2;
   cuuint64_t dims[2] = {uint64_t(cols), uint64_t(rows)};
   cuuint64_t strides[1] = {uint64_t(cols) * esize};
-  cuuint32_t box[2] = {uint32_t(128 / esize), 32};
+  cuuint32_t box[2] = {uint32_t(64 / esize), 32};   // 32 rows x 64 bytes: one epilogue warp's staging block
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

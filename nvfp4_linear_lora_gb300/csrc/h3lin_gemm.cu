@@ -328,21 +328,20 @@ static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t 
 // barrier.
 //   warp 0        producer
 //   warp 1        (leader) MMA issuer
-//   warps 2-7     (leader) scale atoms -> TMEM, two tcgen05.cp each per stage:
-//                 a copy costs its issuing thread a long issue slot, so six
-//                 issuing warps keep the twelve copies of a stage off the
+//   warps 2-7     (leader) scale atoms -> TMEM, two tcgen05.cp each per
+//                 stage: a copy costs its issuing thread a long issue slot, so
+//                 six issuing warps keep the twelve copies of a stage off the
 //                 critical path (they overlap the previous stage's MMAs)
-//   warps 8-15    epilogue: drain TMEM 32 columns at a time, convert (scale,
-//                 SiLU*up, bf16/fp32), stage 32 rows x 128 bytes in a per-warp
-//                 shared scratch and store whole 128-byte lines; the
-//                 accumulator is released as soon as its last columns are in
-//                 registers
-// Copy warps: six for plain tiles; four for SiLU*up tiles, whose epilogue
-// keeps all 128 accumulator columns in registers (more registers per thread).
+//   warps 8-23    epilogue, four per TMEM lane quarter: each warp reads its 32
+//                 rows x 64 accumulator columns (SiLU*up: 32 gate + 32 up) with
+//                 one wait and releases the accumulator at once (the next
+//                 tile's MMAs wait for the slowest warp), then scales /
+//                 applies SiLU*up / converts and stores through a 32 x 64-byte
+//                 staging block per warp with TMA bulk-tensor stores
 template <bool SILU> struct PairRoles {
-  static constexpr int kCpWarps = SILU ? 4 : 6;
+  static constexpr int kCpWarps = 6;
   static constexpr int kEpiWarp0 = 2 + kCpWarps;
-  static constexpr int kThreads = 32 * (kEpiWarp0 + 8);
+  static constexpr int kThreads = 32 * (kEpiWarp0 + 16);
 };
 struct PairCfg {
   static constexpr int kABytes = 128 * 128;
@@ -352,8 +351,8 @@ struct PairCfg {
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;   // 38 KB
   static constexpr int kStages = 5;
   static constexpr int kSfCols = 16 + 32;
-  static constexpr int kEpiWarps = 8;
-  static constexpr int kEpiScratch = 4096;                                          // 32 rows x 128 bytes
+  static constexpr int kEpiWarps = 16;
+  static constexpr int kEpiScratch = 2048;                                          // 32 rows x 64 bytes
   static constexpr int kSmem = kStages * kStageBytes + kEpiWarps * kEpiScratch + 1024 + 256;
   static constexpr int kTmemCols = 512;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -369,9 +368,9 @@ __device__ __forceinline__ float silu_mul_fast(float scale, uint32_t acc_g, uint
   return __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
 }
 
-// The warp's scratch block (32 rows x 128 bytes, 16-byte chunks swizzled by
-// row exactly as the 128-byte TMA swizzle lays them out) -> global through the
-// TMA engine; rows >= M are clipped by the tensor map.
+// The warp's staging block (32 rows x 64 bytes, 16-byte chunks placed as the
+// 64-byte TMA swizzle lays them out) -> global through the TMA engine; rows
+// >= M are clipped by the tensor map.
 __device__ __forceinline__ void epi_store(const CUtensorMap* tm_out, const uint8_t* scratch, int col, int row0,
                                           int lane) {
   fence_proxy_async_smem();
@@ -585,15 +584,13 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quarter of this warp
     const int e = warp - kPairEpiWarp0;
-    const int half = e >> 2;                 // which half of the tile's columns
+    const int c4 = e >> 2;                   // which quarter of the tile's columns
     uint8_t* scratch = epi_scratch + e * C::kEpiScratch;
     const float scale = __fmul_rn(*ts_x, *ts_w);
     const uint32_t leader_tmem_empty = cluster_addr(tmem_empty, 0);
     constexpr int kEsize = F32OUT ? 4 : 2;
-    // rounds of 128-byte row segments: 64 bf16 or 32 fp32 output columns each
-    constexpr int kRoundCols = 128 / kEsize;
-    constexpr int kRounds = (SILU ? 64 : 128) / kRoundCols;
-    static_assert(kRoundCols * kEsize == 128, "128-byte scratch rows");
+    constexpr int kRoundCols = 64 / kEsize;          // output columns per 64-byte staging row
+    constexpr int kRounds = (SILU ? 32 : 64) / kRoundCols;
     uint32_t acc_ph = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
       int tm, tn;
@@ -602,104 +599,40 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
       const int row0 = tm * 256 + 128 * static_cast<int>(crank) + 32 * q;   // first row of this warp
-      const int col0 = SILU ? tn * 128 + half * 64 : tn * 256 + half * 128;
-      if (SILU) {
-        // all 64 gate and 64 up columns of this warp in registers, release the accumulator, then SiLU*up
-        uint32_t g0[32], g1[32], u0[32], u1[32];
-        tmem_ld32(taddr + half * 64, g0);
-        tmem_ld32(taddr + half * 64 + 32, g1);
-        tmem_ld32(taddr + 128 + half * 64, u0);
-        tmem_ld32(taddr + 128 + half * 64 + 32, u1);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
-        // 64 output columns: one 128-byte round (bf16) or two (fp32)
+      const int col0 = SILU ? tn * 128 + c4 * 32 : tn * 256 + c4 * 64;
+      // SiLU*up: a = gate columns c4*32.., b = the matching up columns 128 + c4*32..
+      // otherwise: a, b = accumulator columns c4*64 .. c4*64 + 63
+      uint32_t a[32], b[32];
+      tmem_ld32(taddr + (SILU ? c4 * 32 : c4 * 64), a);
+      tmem_ld32(taddr + (SILU ? 128 + c4 * 32 : c4 * 64 + 32), b);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
 #pragma unroll
-        for (int sr = 0; sr < kRounds; ++sr) {
-          epi_scratch_ready(lane);
+      for (int rd = 0; rd < kRounds; ++rd) {
+        uint32_t w[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (F32OUT) {
-                const int k = 4 * q4 + i;   // column 32 * sr + k
-                w[i] = __float_as_uint(silu_mul_fast(scale, sr ? g1[k] : g0[k], sr ? u1[k] : u0[k]));
-              } else {
-                const int col = 8 * q4 + 2 * i;
-                const uint32_t ga = col < 32 ? g0[col] : g1[col - 32], ua = col < 32 ? u0[col] : u1[col - 32];
-                const uint32_t gb = col < 32 ? g0[col + 1] : g1[col - 31], ub = col < 32 ? u0[col + 1] : u1[col - 31];
-                w[i] = pack_bf16x2(silu_mul_fast(scale, ga, ua), silu_mul_fast(scale, gb, ub));
-              }
-            }
-            *reinterpret_cast<uint4*>(scratch + lane * 128 + ((q4 ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          epi_store(&tm_out, scratch, col0 + sr * kRoundCols, row0, lane);
-        }
-      } else if (!F32OUT) {
-        // bf16: pack all 128 columns of this warp into 64 registers, release the
-        // accumulator, then stage and store two 64-column rounds
-        // two loads in flight per wait: columns 0-63, then 64-127 (released right after)
-        uint32_t w[64];
-        {
-          uint32_t a0[32], a1[32];
-          tmem_ld32(taddr + half * 128, a0);
-          tmem_ld32(taddr + half * 128 + 32, a1);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            w[i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a0[2 * i])), __fmul_rn(scale, __uint_as_float(a0[2 * i + 1])));
-            w[16 + i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a1[2 * i])), __fmul_rn(scale, __uint_as_float(a1[2 * i + 1])));
+        for (int k = 0; k < 16; ++k) {
+          if (F32OUT) {
+            const int c = rd * 16 + k;   // output column of this warp
+            w[k] = SILU ? __float_as_uint(silu_mul_fast(scale, a[c], b[c]))
+                        : __float_as_uint(__fmul_rn(scale, __uint_as_float(c < 32 ? a[c] : b[c - 32])));
+          } else if (SILU) {
+            w[k] = pack_bf16x2(silu_mul_fast(scale, a[2 * k], b[2 * k]), silu_mul_fast(scale, a[2 * k + 1], b[2 * k + 1]));
+          } else {
+            const int c = rd * 32 + 2 * k;
+            const uint32_t lo = c < 32 ? a[c] : b[c - 32], hi = c < 32 ? a[c + 1] : b[c - 31];
+            w[k] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(lo)), __fmul_rn(scale, __uint_as_float(hi)));
           }
         }
-        {
-          uint32_t a2[32], a3[32];
-          tmem_ld32(taddr + half * 128 + 64, a2);
-          tmem_ld32(taddr + half * 128 + 96, a3);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+        epi_scratch_ready(lane);
+        // row = lane, 64 bytes; 16-byte chunks placed as the 64-byte TMA swizzle expects
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            w[32 + i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a2[2 * i])), __fmul_rn(scale, __uint_as_float(a2[2 * i + 1])));
-            w[48 + i] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(a3[2 * i])), __fmul_rn(scale, __uint_as_float(a3[2 * i + 1])));
-          }
-        }
-#pragma unroll
-        for (int rd = 0; rd < 2; ++rd) {
-          epi_scratch_ready(lane);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(scratch + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                make_uint4(w[rd * 32 + 4 * c], w[rd * 32 + 4 * c + 1], w[rd * 32 + 4 * c + 2], w[rd * 32 + 4 * c + 3]);
-          epi_store(&tm_out, scratch, col0 + rd * 64, row0, lane);
-        }
-      } else {
-        // fp32 (checking mode): rounds of 32 columns; the accumulator is released
-        // after the last round's columns are in registers
-        uint32_t w[32];
-#pragma unroll 1
-        for (int rd = 0; rd < kRounds; ++rd) {
-          uint32_t a[32];
-          tmem_ld32(taddr + half * 128 + rd * 32, a);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__fmul_rn(scale, __uint_as_float(a[i])));
-          if (rd == kRounds - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
-          }
-          epi_scratch_ready(lane);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(scratch + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-          epi_store(&tm_out, scratch, col0 + rd * 32, row0, lane);
-        }
-        __syncwarp();
+        for (int ch = 0; ch < 4; ++ch)
+          *reinterpret_cast<uint4*>(scratch + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) =
+              make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+        epi_store(&tm_out, scratch, col0 + rd * kRoundCols, row0, lane);
       }
       acc_ph ^= 1;
     }
