@@ -228,11 +228,15 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant(
 }
 
 // ------------------------------------------------------------- k_amax_lora
-// Warp 0: TMA producer.  Warp 1: TMEM owner + MMA issuer.  Warps 2-5: amax of
+// Warp 0: TMA producer.  Warp 1: TMEM owner + MMA issuer.  Warps 2-9: amax of
 // |x * s| read from the staged tile, then the epilogue u = bf16(TMEM).
 // One 128-row tile of x per CTA iteration; K in 64-column stages (x tile
 // 128 x 64 bf16 = 16 KB, A tile rank x 64 bf16), 128-byte swizzle.
-constexpr int kLoraThreads = 192;
+// Amax thread a (0..255) owns the 16-byte column chunk a % 8 of rows
+// a / 8 + 32 i (i = 0..3) of every stage, so its 8 per-channel scales are two
+// loads per stage.
+constexpr int kLoraAmaxWarps = 8;
+constexpr int kLoraThreads = 64 + 32 * kLoraAmaxWarps;
 
 __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a, int M, int K,
@@ -254,10 +258,10 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4);
+      mbar_init(&empty[s], 1 + kLoraAmaxWarps);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 4);
+    mbar_init(tmem_empty, kLoraAmaxWarps);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -333,28 +337,27 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
       mbar_drain(drain_bar, 0);
     }
   } else {
-    // amax + epilogue warps; warp w reads TMEM lanes 32 * (w % 4) ...
+    // amax + epilogue warps.  TMEM access: warp w reads lanes 32 * (w % 4) ..;
+    // the two warps of a lane quarter take alternate 32-column chunks of u.
+    const int aw = warp - 2;                 // 0 .. kLoraAmaxWarps - 1
+    const int at = threadIdx.x - 64;         // amax thread
+    const int ch = at & 7;                   // 16-byte column chunk
+    const int rb = at >> 3;                  // first row (0..31)
     const int q = warp & 3;
-    const int rl = 32 * q + lane;  // row inside the tile
+    const int half = aw >> 2;
     float m = 0.0f;
     int st = 0;
     uint32_t ph = 0, acc_ph = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       for (int kc = 0; kc < nk; ++kc) {
+        float s[8];
+        load_scale8(pqs, kc * 8 + ch, s);
         if (!mbar_wait(&full[st], ph, ab)) goto amax_done;
-        const uint8_t* rowp = smem + st * stage_bytes + rl * 128;
-        const float4* sp = pqs ? reinterpret_cast<const float4*>(pqs + kc * 64) : nullptr;
+        const uint8_t* tile = smem + st * stage_bytes;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((j ^ (rl & 7)) << 4));
-          float s[8];
-          if (sp) {
-            const float4 a = __ldg(sp + 2 * j), b = __ldg(sp + 2 * j + 1);
-            s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w; s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) s[i] = 1.0f;
-          }
+        for (int i = 0; i < 4; ++i) {
+          const int r = rb + 32 * i;
+          const uint4 w = *reinterpret_cast<const uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4));
           float v[8];
           prescale8(w, s, v);
           m = fmaxf(m, absmax8(v));
@@ -367,9 +370,9 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
       if (!mbar_wait(tmem_full, acc_ph, ab)) goto amax_done;
       tc_fence_after();
       {
-        const int row = t * 128 + rl;
+        const int row = t * 128 + 32 * q + lane;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        for (int c0 = 0; c0 < rank; c0 += 32) {
+        for (int c0 = 32 * half; c0 < rank; c0 += 64) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           tmem_ld_wait();
@@ -395,11 +398,15 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
   amax_done:
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) red[q] = m;
+    if (lane == 0) red[aw] = m;
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) partials[blockIdx.x] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  if (threadIdx.x == 0) {
+    float m = red[0];
+    for (int i = 1; i < kLoraAmaxWarps; ++i) m = fmaxf(m, red[i]);
+    partials[blockIdx.x] = m;
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols);
@@ -469,7 +476,7 @@ cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, i
   const int stage_bytes = 16384 + rank * 128;
   constexpr int kSmemLimit = 232448;
   int stages = (kSmemLimit - 1024 - 256) / stage_bytes;
-  if (stages > 6) stages = 6;
+  if (stages > 8) stages = 8;
   if (stages < 2) return cudaErrorInvalidValue;
   const int smem = stages * stage_bytes + 1024 + 256;
   int tmem_cols = 32;
