@@ -43,12 +43,33 @@ __device__ __forceinline__ void prescale8(const uint4& w, const float (&s)[8], f
   v[7] = __fmul_rn(bf16hi(w.w), s[7]);
 }
 
-__device__ __forceinline__ float absmax8(const float (&v)[8]) {
-  float m = fabsf(v[0]);
+// max |x * s| over rows, without a multiply per element: rounding is monotone,
+// so max_r |fl(x_r * s)| = fl(max_r |x_r| * |s|) exactly.  The column-wise
+// max |x| is kept as four bf16 pairs (NaN operands are skipped, as fmaxf
+// skips them), and scaled once per column.
+struct ColMax8 {
+  __nv_bfloat162 h[4];
+  __device__ __forceinline__ ColMax8() {
 #pragma unroll
-  for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
-  return m;
-}
+    for (int i = 0; i < 4; ++i) h[i] = __float2bfloat162_rn(0.0f);
+  }
+  __device__ __forceinline__ void add(const uint4& w) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __hmax2(h[i], __habs2(*reinterpret_cast<const __nv_bfloat162*>(&u[i])));
+  }
+  // max over the 8 columns of |colmax * s|
+  __device__ __forceinline__ float scaled_max(const float (&s)[8]) const {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(&h[i]);
+      m = fmaxf(m, __fmul_rn(bf16lo(u), fabsf(s[2 * i])));
+      m = fmaxf(m, __fmul_rn(bf16hi(u), fabsf(s[2 * i + 1])));
+    }
+    return m;
+  }
+};
 
 // Block-wide max; every thread gets the result.
 __device__ __forceinline__ float block_max(float m, float* red) {
@@ -74,23 +95,18 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict_
   const int r0 = tid / kc;
   float m = 0.0f;
   if (r0 < rows_step) {
-    float s[8];
-    load_scale8(pqs, c, s);
+    ColMax8 cm;
     int row = r0;
     for (; row + rows_step < M; row += 2 * rows_step) {
       const uint4 a = x[static_cast<int64_t>(row) * kc + c];
       const uint4 b = x[static_cast<int64_t>(row + rows_step) * kc + c];
-      float v[8];
-      prescale8(a, s, v);
-      m = fmaxf(m, absmax8(v));
-      prescale8(b, s, v);
-      m = fmaxf(m, absmax8(v));
+      cm.add(a);
+      cm.add(b);
     }
-    if (row < M) {
-      float v[8];
-      prescale8(x[static_cast<int64_t>(row) * kc + c], s, v);
-      m = fmaxf(m, absmax8(v));
-    }
+    if (row < M) cm.add(x[static_cast<int64_t>(row) * kc + c]);
+    float s[8];
+    load_scale8(pqs, c, s);
+    m = cm.scaled_max(s);
   }
   m = block_max(m, red);
   if (threadIdx.x == 0) partials[blockIdx.x] = m;
@@ -232,10 +248,12 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant(
 // |x * s| read from the staged tile, then the epilogue u = bf16(TMEM).
 // One 128-row tile of x per CTA iteration; K in 64-column stages (x tile
 // 128 x 64 bf16 = 16 KB, A tile rank x 64 bf16), 128-byte swizzle.
-// Amax thread a (0..255) owns the 16-byte column chunk a % 8 of rows
-// a / 8 + 32 i (i = 0..3) of every stage, so its 8 per-channel scales are two
+// Amax thread a owns the 16-byte column chunk a % 8 of rows a / 8 + R i
+// (R = 32 * warps / 8) of every stage, so its 8 per-channel scales are two
 // loads per stage.
 constexpr int kLoraAmaxWarps = 8;
+constexpr int kLoraRowStride = 32 * kLoraAmaxWarps / 8;   // rows between a thread's rows
+static_assert(128 % kLoraRowStride == 0, "rows of a tile per amax thread");
 constexpr int kLoraThreads = 64 + 32 * kLoraAmaxWarps;
 
 __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
@@ -338,30 +356,43 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
     }
   } else {
     // amax + epilogue warps.  TMEM access: warp w reads lanes 32 * (w % 4) ..;
-    // the two warps of a lane quarter take alternate 32-column chunks of u.
+    // the warps of a lane quarter take interleaved 32-column chunks of u.
     const int aw = warp - 2;                 // 0 .. kLoraAmaxWarps - 1
     const int at = threadIdx.x - 64;         // amax thread
     const int ch = at & 7;                   // 16-byte column chunk
-    const int rb = at >> 3;                  // first row (0..31)
+    const int rb = at >> 3;                  // first row
     const int q = warp & 3;
-    const int half = aw >> 2;
+    const int part = aw >> 2;                // 0 .. kLoraAmaxWarps / 4 - 1
+    constexpr int kParts = kLoraAmaxWarps / 4;
     float m = 0.0f;
     int st = 0;
     uint32_t ph = 0, acc_ph = 0;
+    // The per-channel scales of a stage are loaded two stages ahead: the
+    // shared-memory ring leaves little L1, so these loads go to L2.
+    float s0[8], s1[8];
+    load_scale8(pqs, ch, s0);
+    load_scale8(pqs, (nk > 1 ? 1 : 0) * 8 + ch, s1);
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       for (int kc = 0; kc < nk; ++kc) {
-        float s[8];
-        load_scale8(pqs, kc * 8 + ch, s);
+        float s[8], s2[8];
+        int k2 = kc + 2;
+        while (k2 >= nk) k2 -= nk;
+        load_scale8(pqs, k2 * 8 + ch, s2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          s[i] = s0[i];
+          s0[i] = s1[i];
+          s1[i] = s2[i];
+        }
         if (!mbar_wait(&full[st], ph, ab)) goto amax_done;
         const uint8_t* tile = smem + st * stage_bytes;
+        ColMax8 cm;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = rb + 32 * i;
-          const uint4 w = *reinterpret_cast<const uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4));
-          float v[8];
-          prescale8(w, s, v);
-          m = fmaxf(m, absmax8(v));
+        for (int i = 0; i < 128 / kLoraRowStride; ++i) {
+          const int r = rb + kLoraRowStride * i;
+          cm.add(*reinterpret_cast<const uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4)));
         }
+        m = fmaxf(m, cm.scaled_max(s));
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         if (++st == stages) { st = 0; ph ^= 1; }
@@ -372,7 +403,7 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
       {
         const int row = t * 128 + 32 * q + lane;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        for (int c0 = 32 * half; c0 < rank; c0 += 64) {
+        for (int c0 = 32 * part; c0 < rank; c0 += 32 * kParts) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           tmem_ld_wait();
