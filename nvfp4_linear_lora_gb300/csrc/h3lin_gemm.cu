@@ -457,6 +457,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     if (lane == 0) {
       int st = 0;
       uint32_t ph = 0;
+      uint32_t filled = 0, fill_par = 0;   // leader: slots with a fill expected on full[], and its phase
       for (int t = pair; t < num_tiles; t += npairs) {
         int tm, tn;
         tile_coords(t, tiles_m, tiles_n, tm, tn);
@@ -468,7 +469,11 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
           if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
           uint8_t* base = smem + st * C::kStageBytes;
           const uint32_t lbar = cluster_addr(&full[st], 0);
-          if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::kStageBytes);
+          if (leader) {
+            mbar_arrive_expect_tx(&full[st], 2 * C::kStageBytes);
+            filled |= 1u << st;
+            fill_par = (fill_par & ~(1u << st)) | (ph << st);
+          }
           tma_load_2d_pair(base, &tm_xq, lbar, kc * 128, m0);
           tma_load_2d_pair(base + C::kABytes, &tm_wq, lbar, kc * 128, brow);
           tma_load_2d_pair(base + C::kABytes + C::kBBytes, &tm_xs, lbar, 0, 2 * ((m0 >> 7) * k_atoms + kc * 4));
@@ -482,13 +487,23 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
           if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
           uint8_t* base = smem + st * C::kStageBytes;
           const uint32_t lbar = cluster_addr(&full[st], 0);
-          if (leader) mbar_arrive_expect_tx(&full[st], 2 * (C::kABytes + C::kBBytes));
+          if (leader) {
+            mbar_arrive_expect_tx(&full[st], 2 * (C::kABytes + C::kBBytes));
+            filled |= 1u << st;
+            fill_par = (fill_par & ~(1u << st)) | (ph << st);
+          }
           tma_load_2d_pair(base, &tm_u, lbar, rc * 64, m0);
           tma_load_2d_pair(base + C::kABytes, &tm_b, lbar, rc * 64, brow);
           if (++st == C::kStages) { st = 0; ph ^= 1; }
         }
       }
-    producer_done:;
+    producer_done:
+      // Both CTAs' loads of a stage complete on the leader's full barrier: before
+      // this CTA pair can exit (after an abort, too) the leader waits, bounded,
+      // for every fill it expected.  After a normal run these have all completed.
+      if (leader)
+        for (int s2 = 0; s2 < C::kStages; ++s2)
+          if (filled & (1u << s2)) mbar_drain(&full[s2], (fill_par >> s2) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
