@@ -30,6 +30,38 @@ sys.path.insert(0, ROOT)
 
 from nvfp4_linear_lora_gb300 import configs, synth  # noqa: E402
 
+
+# DRAM traffic of the GEMM launches (dram__bytes_read.sum + dram__bytes_write.sum
+# per launch) from one ncu capture of the S=37726 block, summarised in
+# profiles/dram_fp4gemm_pair_S37726.md.  It is reported only while the GEMM
+# sources hash to the value the capture was taken with; after any change to
+# them the counters no longer describe the kernel and `traffic` is null.
+GEMM_TRAFFIC = {"sources_sha256": "074ccd897e03884ab4a379b8178b0994b35762eb6409fec98af6cfa2a1ac9dc7", "S": 37726,
+                "bytes_per_launch": {"qkv": 499579392 + 1119095552, "attn_out": 134761984 + 338764288,
+                                     "gate_up": 561148160 + 1007247360, "down": 531803904 + 368068352}}
+GEMM_SOURCES = ("nvfp4_linear_lora_gb300/csrc/h3lin_gemm.cu", "nvfp4_linear_lora_gb300/csrc/h3lin_device.cuh",
+                "nvfp4_linear_lora_gb300/csrc/h3lin_api.cu")
+
+
+def gemm_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    here = os.path.dirname(os.path.abspath(__file__))
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(here, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_algorithmic_bytes(S):
+    """Bytes one GEMM launch must move at least: x codes + scales, W codes +
+    scales, u and B' (bf16), the bf16 output."""
+    out = {}
+    for name, K, N, r, silu in configs.BLOCK_PROJECTIONS:
+        n_out = N // 2 if silu else N
+        out[name] = S * K // 2 + S * K // 16 + N * K // 2 + N * K // 16 + 2 * S * r + 2 * N * r + 2 * S * n_out
+    return out
+
 METRIC = "NVFP4+LoRA projection TFLOP/s at S=37726 (% of dense FP4 peak); ms/block"
 FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor ratio on GB300
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -390,8 +422,16 @@ def native_arm(a, rank, world, local_rank):
     ideal_s = gemm_fp4 / (peak_fp4 * 1e12) + gemm_bf16 / (peak_bf16 * 1e12)
     mixed_peak = (gemm_fp4 + gemm_bf16) / ideal_s / 1e12
     achieved = (gemm_fp4 + gemm_bf16) / (gemm_total_ms * 1e-3) / 1e12
+    alg = gemm_algorithmic_bytes(S)
+    traffic = None
+    if GEMM_TRAFFIC["sources_sha256"] == gemm_sources_sha256() and GEMM_TRAFFIC["S"] == S:
+        traffic = sum(GEMM_TRAFFIC["bytes_per_launch"].values())
     roofline = {"kernel": "k_fp4gemm", "bound": "tensor", "achieved": achieved, "peak": mixed_peak,
-                "unit": "TFLOP/s", "frac": achieved / mixed_peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / mixed_peak, "traffic": traffic,
+                "traffic_scope": "DRAM bytes of the block's four GEMM launches (read + write), as achieved is "
+                                 "the FLOPs of those four launches over their summed time",
+                "algorithmic_bytes": sum(alg.values()),
+                "traffic_per_launch": dict(GEMM_TRAFFIC["bytes_per_launch"]) if traffic else None,
                 "peak_basis": f"{peak_kind} sustained bf16 {peak_bf16:.1f} TF/s x {FP4_OVER_BF16:g} for the FP4 "
                               f"part, x 1 for the BF16 LoRA-up part, time-weighted over this kernel's FLOP mix",
                 "gemm_ms_per_projection": dict(zip([d["name"] for d in blk.proj], gemm_ms))}

@@ -260,6 +260,23 @@ h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
   return H3LIN_OK;
 }
 
+// M-tiles per raster group of the GEMM.  A narrow weight (N <= 8192, packed
+// codes and scales <= 48 MB) stays resident in L2 while its few N tiles are
+// swept, so the raster runs N-fastest and every x panel is read from HBM once
+// (measured on the block: attn-out and down GEMM reads drop from 0.21 and 1.79
+// GB to 0.13 and 0.54 GB).  A wide weight (QKV, gate/up) is evicted by the
+// output streaming through L2 between its reuses; there a group keeps about
+// 24 MB of x panels in L2 while the weight panels pass.
+int raster_group(int64_t N, int64_t K, int tile_rows) {
+  const int64_t weight_bytes = N * (K / 2) + N * (K / 16);
+  if (N <= 8192 && weight_bytes <= (int64_t(48) << 20)) return 1;
+  const int64_t panel = int64_t(tile_rows) * (K / 2);
+  int64_t g = (int64_t(24) << 20) / (panel > 0 ? panel : 1);
+  if (g < 1) g = 1;
+  if (g > 32) g = 32;
+  return int(g);
+}
+
 // FP4 GEMM + LoRA-up + epilogue reading the prepared workspace.
 h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream) {
   GemmArgs g;
@@ -296,6 +313,7 @@ h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream) {
            make_sf_map(&g.tm_xs, g.xs, size_t((c.M + 127) / 128 * 128) * size_t(c.K / 16)) &&
            make_sf_map(&g.tm_ws, g.ws, size_t(c.N) * size_t(c.K / 16)) &&
            make_out_map(&g.tm_out, c.out, c.f32out, g.ldo, c.M);
+  g.group_m = raster_group(c.N, c.K, g.pair ? 256 : 128);
   if (launch_fp4gemm(g, c.dev.sm_count, stream) != cudaSuccess) return H3LIN_E_CUDA;
   return H3LIN_OK;
 }

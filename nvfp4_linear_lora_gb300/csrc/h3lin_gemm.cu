@@ -27,7 +27,6 @@
 namespace h3lin {
 
 constexpr int kGemmThreads = 320;
-constexpr int kGroupM = 32;
 
 template <int BN>
 struct GemmCfg {
@@ -44,12 +43,17 @@ struct GemmCfg {
   static_assert(BN + kStages * kSfCols <= kTmemCols, "TMEM budget");
 };
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
-  const int per_group = kGroupM * tiles_n;
+// Tile t -> (tm, tn), rastered in groups of group_m M-tiles: within a group
+// the M index moves fastest, so a group's panel of x (group_m tiles) stays in
+// L2 while the weight panels stream past it.  group_m = 1 is N-fastest: each
+// x panel is read once and the whole weight stays L2-resident (chosen on the
+// host when the packed weight is small enough).
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int& tm, int& tn) {
+  const int per_group = group_m * tiles_n;
   const int g = t / per_group;
   const int r = t - g * per_group;
-  const int gm = min(kGroupM, tiles_m - g * kGroupM);
-  tm = g * kGroupM + r % gm;
+  const int gm = min(group_m, tiles_m - g * group_m);
+  tm = g * group_m + r % gm;
   tn = r / gm;
 }
 
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
     const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_wq,
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_b,
     const uint8_t* __restrict__ xs, const uint8_t* __restrict__ ws, const float* __restrict__ ts_x,
-    const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K, int rank, int ldo,
+    const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K, int rank, int ldo, int group_m,
     uint32_t* __restrict__ status) {
   using C = GemmCfg<BN>;
   static_assert(!SILU || BN == 256, "SiLU*up pairs 128 gate and 128 up columns");
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
       uint32_t ph = 0;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         int tm, tn;
-        tile_coords(t, tiles_m, tiles_n, tm, tn);
+        tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
         const int m0 = tm * 128;
         int brow[2];
         if (SILU) {
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       int tm, tn;
-      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
       if (!mbar_wait(tmem_full, acc_ph, ab)) break;
       tc_fence_after();
       const int row = tm * 128 + 32 * q + lane;
@@ -314,7 +318,7 @@ static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t 
   const int tiles = tiles_m * tiles_n;
   const int grid = tiles < sm_count ? tiles : sm_count;
   kern<<<grid, kGemmThreads, C::kSmem, st>>>(a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.xs, a.ws, a.ts_x, a.ts_w,
-                                             a.out, a.M, a.N, a.K, a.rank, a.ldo,
+                                             a.out, a.M, a.N, a.K, a.rank, a.ldo, a.group_m,
                                              a.status);
   return cudaGetLastError();
 }
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_ws,
     const __grid_constant__ CUtensorMap tm_out,
     const float* __restrict__ ts_x, const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K,
-    int rank, int ldo, uint32_t* __restrict__ status) {
+    int rank, int ldo, int group_m, uint32_t* __restrict__ status) {
   using C = PairCfg;
   constexpr int kPairCpWarps = PairRoles<SILU>::kCpWarps;
   constexpr int kPairEpiWarp0 = PairRoles<SILU>::kEpiWarp0;
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
       uint32_t filled = 0, fill_par = 0;   // leader: slots with a fill expected on full[], and its phase
       for (int t = pair; t < num_tiles; t += npairs) {
         int tm, tn;
-        tile_coords(t, tiles_m, tiles_n, tm, tn);
+        tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
         const int m0 = tm * 256 + 128 * static_cast<int>(crank);
         const int h0 = SILU ? tn * 128 : tn * 256;              // B rows of the tile's two halves
         const int h1 = SILU ? N / 2 + tn * 128 : tn * 256 + 128;
@@ -609,7 +613,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     uint32_t acc_ph = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
       int tm, tn;
-      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
       if (!mbar_wait(tmem_full, acc_ph, ab)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
@@ -686,7 +690,7 @@ static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStre
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.tm_xs, a.tm_ws, a.tm_out, a.ts_x, a.ts_w,
-                            a.out, a.M, a.N, a.K, a.rank, a.ldo, a.status);
+                            a.out, a.M, a.N, a.K, a.rank, a.ldo, a.group_m, a.status);
 }
 
 template <bool F32OUT>

@@ -51,6 +51,7 @@ struct GemmArgs {
   const float* ts_w;
   void* out;
   int M, N, K, rank, ldo;
+  int group_m;                // M-tiles per raster group (1 = N-fastest)
   uint32_t* status;
   bool lora, silu, f32out;
   bool pair;                  // use the CTA-pair kernel
