@@ -10,9 +10,13 @@ list "The rest.", item "Backbone": the LoRA's update is merged before
 quantizing), as a comparison point for the dynamic path, whose LoRA branch
 stays separate (TURBO.md, h3-blackwell-runtime, "Implementation"):
 
-    W' = bf16( W + strength * (alpha / rank) * (B @ A) )
+    W' = bf16( W + strength * (alpha / rank) * (B @ A) / s )
 
-with ``W [N, K]``, ``B [N, r]``, ``A [r, K]`` holding bf16 values.  The sum is
+with ``W [N, K]``, ``B [N, r]``, ``A [r, K]`` holding bf16 values and ``s``
+the per-input-channel ``pre_quant_scale`` (1 when absent).  The base branch
+computes ``(x * s) @ W.T`` while the LoRA branch sees the original ``x``
+(TURBO.md, "Implementation"), so the folded update carries ``1 / s`` for
+``(x * s) @ W'.T`` to reproduce ``x @ (B A).T``.  The sum is
 formed in float64 (each product of two bf16 values is exact and r <= 512 terms
 of such products lose nothing), then rounded once to bf16, to nearest with
 ties to even.  ``W'`` is then packed like any weight (``linear.pack_weight``).
@@ -36,10 +40,13 @@ def bf16_rne(a) -> np.ndarray:
     return out.astype(np.float32)
 
 
-def merge_lora(W, A, B, alpha, rank, strength) -> np.ndarray:
-    """``bf16(W + strength * (alpha/rank) * B @ A)`` as float32 [N, K]."""
+def merge_lora(W, A, B, alpha, rank, strength, pre_quant_scale=None) -> np.ndarray:
+    """``bf16(W + strength * (alpha/rank) * B @ A / s)`` as float32 [N, K]."""
     W = np.asarray(W, dtype=np.float64)
     A = np.asarray(A, dtype=np.float64)
     B = np.asarray(B, dtype=np.float64)
     c = float(strength) * (float(alpha) / float(rank))
-    return bf16_rne(W + c * (B @ A))
+    upd = c * (B @ A)
+    if pre_quant_scale is not None:
+        upd = upd / np.asarray(pre_quant_scale, dtype=np.float64)[None, :]
+    return bf16_rne(W + upd)

@@ -104,3 +104,21 @@ def test_merge_special_cases():
     a = merged.merge_lora(W * 0, A, B, 8.0, r, 0.5)
     b = merged.merge_lora(W * 0, A, B, 4.0, r, 1.0)
     assert np.array_equal(a, b)
+
+
+def test_merge_divides_the_update_by_the_pre_quant_scale():
+    rng = np.random.default_rng(4)
+    N, K, r = 6, 8, 2
+    W = _bf16_values(rng, (N, K), 0.1)
+    A = _bf16_values(rng, (r, K))
+    B = _bf16_values(rng, (N, r))
+    s = np.array([2.0, 0.5, 1.0, 4.0, 0.25, 1.0, 2.0, 0.5], np.float32)   # powers of two: exact division
+    got = merged.merge_lora(W, A, B, 2.0, r, 1.0, s)
+    want = merged.merge_lora(W, A / s[None, :], B, 2.0, r, 1.0)
+    assert np.array_equal(got, want)
+    # without rounding, (x * s) @ W'.T = (x * s) @ W.T + x @ (c B A).T
+    x = rng.standard_normal((3, K))
+    upd = (1.0 * (B.astype(np.float64) @ A.astype(np.float64))) / s[None, :]
+    lhs = (x * s) @ (W.astype(np.float64) + upd).T
+    rhs = (x * s) @ W.astype(np.float64).T + x @ (B.astype(np.float64) @ A.astype(np.float64)).T
+    assert np.allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
