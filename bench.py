@@ -36,11 +36,10 @@ from nvfp4_linear_lora_gb300 import configs, synth  # noqa: E402
 # profiles/dram_fp4gemm_pair_S37726.md.  It is reported only while the GEMM
 # sources hash to the value the capture was taken with; after any change to
 # them the counters no longer describe the kernel and `traffic` is null.
-GEMM_TRAFFIC = {"sources_sha256": "074ccd897e03884ab4a379b8178b0994b35762eb6409fec98af6cfa2a1ac9dc7", "S": 37726,
+GEMM_TRAFFIC = {"sources_sha256": "6bdb56da4c4ceb71dd9df92f0100861ab052832eae3c7a69b1d77857f12f9f57", "S": 37726,
                 "bytes_per_launch": {"qkv": 499579392 + 1119095552, "attn_out": 134761984 + 338764288,
                                      "gate_up": 561148160 + 1007247360, "down": 531803904 + 368068352}}
-GEMM_SOURCES = ("nvfp4_linear_lora_gb300/csrc/h3lin_gemm.cu", "nvfp4_linear_lora_gb300/csrc/h3lin_device.cuh",
-                "nvfp4_linear_lora_gb300/csrc/h3lin_api.cu")
+GEMM_SOURCES = ("nvfp4_linear_lora_gb300/csrc/h3lin_gemm.cu", "nvfp4_linear_lora_gb300/csrc/h3lin_device.cuh")
 
 
 def gemm_sources_sha256():
@@ -77,6 +76,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-merged", action="store_true",
+                    help="skip the merged-LoRA comparison (weights with the adapter folded in, base path only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU-oracle sample time")
     return ap.parse_args(argv)
 
@@ -394,6 +395,57 @@ def native_arm(a, rank, world, local_rank):
         ms = float(t.item())
     value = world * total / (ms * 1e-3) / 1e12
 
+    # merged-LoRA comparison mode: each weight with its adapter folded in
+    # (h3lin_merge_lora), re-packed, then the block on the base path only
+    merged_line = None
+    if not a.no_merged:
+        h3 = blk.h3lin
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        packed_m = []
+        merge_ms = 0.0
+        for p, d in zip(host, blk.proj):
+            Wd = synth.to_bf16_tensor(p["W"]).to(device)
+            m0.record()
+            h3.merge_lora(Wd, d["ad"], 1.0, d["pqs_dev"], out=Wd)
+            pwm = h3.pack_weight(Wd)
+            m1.record()
+            torch.cuda.synchronize()
+            merge_ms += m0.elapsed_time(m1)
+            del Wd
+            packed_m.append(pwm)
+        saved = [(d["wc"], d["ac"]) for d in blk.proj]
+        for d, pwm in zip(blk.proj, packed_m):
+            d["wc"], d["ac"] = pwm.c_struct(), None
+        try:
+            for _ in range(a.warmup):
+                blk.step()
+            torch.cuda.synchronize()
+            n_m = max(10, a.steps // 4)
+            barrier()
+            torch.cuda.synchronize()
+            t0.record()
+            for _ in range(n_m):
+                blk.step()
+            t1.record()
+            torch.cuda.synchronize()
+            barrier()
+            mms = t0.elapsed_time(t1) / n_m
+            blk.check_status()
+        finally:
+            for d, (wc, ac) in zip(blk.proj, saved):
+                d["wc"], d["ac"] = wc, ac
+        if world > 1:
+            t = torch.tensor([mms], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            mms = float(t.item())
+        merged_line = {"ms_per_block": mms, "steps": n_m,
+                       "base_tflops": world * base / (mms * 1e-3) / 1e12,
+                       "dynamic_over_merged_time": ms / mms,
+                       "merge_and_pack_ms": merge_ms,
+                       "what": "adapter folded into each weight (h3lin_merge_lora, strength 1) and re-packed; "
+                               "the block then runs the base path only (adapter NULL). A speed bound for the "
+                               "dynamic path, paid for by re-packing per adapter/strength switch"}
+
     # end to end through the C ABI from pinned host buffers
     e2e = None
     if not a.no_e2e:
@@ -494,7 +546,7 @@ def native_arm(a, rank, world, local_rank):
             "ms_per_block": ms, "frac_of_fp4_peak": value / world / peak_fp4,
             "flops_per_block": {"total": total, "base_fp4": base, "lora_down": ldown, "lora_up": lup},
             "kernel_ms": {"gemm": gemm_total_ms, "prepare": ms - gemm_total_ms},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "merged_lora": merged_line,
             "gpu_launches": blk.launches_per_step() * a.steps, "clocks": clocks,
             "peaks": {"kind": peak_kind, **peaks}}
     print(json.dumps(line), flush=True)

@@ -173,6 +173,34 @@ h3lin_status h3lin_forward_gemm(int64_t M, const h3lin_weight* weight, int32_t e
                                 const h3lin_adapter* adapter, float strength, void* out, int32_t out_dtype,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------ merged-LoRA weights */
+/* Comparison mode of the dynamic path: the LoRA update folded into the
+ * weight before it is packed (MiniMax-H3 Turbo — one file, no Python, "What
+ * the conversion did", list "The rest.", item "Backbone": the LoRA update is
+ * merged before quantizing).
+ *
+ *   w_out[n, k] = bf16_rn( w[n, k] + strength * (alpha / rank) * (sum_j B[n, j] * A[j, k]) / s[k] )
+ *
+ * with FP32 fused multiply-adds over j in ascending order and one rounding to
+ * bf16 at the end.  s is the pre_quant_scale the forward will be called with
+ * (1 when NULL): the base branch quantises x * s while the LoRA branch sees x
+ * (TURBO.md, h3-blackwell-runtime, "Implementation"), so the folded update is
+ * divided by s.  Pack the result with h3lin_pack_weight and run
+ * h3lin_forward with adapter == NULL: that forward costs only the base path,
+ * the speed bound of the dynamic one, at the price of re-packing the weight
+ * for every adapter or strength.
+ *   w        device bf16 [N, K], row-major; 8-byte aligned
+ *   pre_quant_scale  device fp32 [K] or NULL; 16-byte aligned
+ *   adapter  the adapter (A bf16 [rank, K], B bf16 [N, rank]); rank rule as
+ *            for h3lin_forward
+ *   w_out    device bf16 [N, K], 8-byte aligned; may equal w (in place)
+ * K must be a multiple of 64.  Errors: H3LIN_E_INVALID (null pointers,
+ * non-finite alpha or strength), H3LIN_E_SHAPE (N, K or rank),
+ * H3LIN_E_ALIGN, H3LIN_E_UNSUPPORTED, H3LIN_E_CUDA; nothing is enqueued on
+ * error.  Allocates nothing. */
+h3lin_status h3lin_merge_lora(const void* w, int64_t N, int64_t K, const float* pre_quant_scale,
+                              const h3lin_adapter* adapter, float strength, void* w_out, cudaStream_t stream);
+
 /* ------------------------------------------------------- failure self-test */
 /* Exercises the kernels' failure path on the device without any fault: a
  * kernel waits, with a bound of `wait_cycles` SM clock cycles (1 .. 2^31), on

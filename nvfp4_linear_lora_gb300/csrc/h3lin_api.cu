@@ -260,23 +260,6 @@ h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
   return H3LIN_OK;
 }
 
-// M-tiles per raster group of the GEMM.  A narrow weight (N <= 8192, packed
-// codes and scales <= 48 MB) stays resident in L2 while its few N tiles are
-// swept, so the raster runs N-fastest and every x panel is read from HBM once
-// (measured on the block: attn-out and down GEMM reads drop from 0.21 and 1.79
-// GB to 0.13 and 0.54 GB).  A wide weight (QKV, gate/up) is evicted by the
-// output streaming through L2 between its reuses; there a group keeps about
-// 24 MB of x panels in L2 while the weight panels pass.
-int raster_group(int64_t N, int64_t K, int tile_rows) {
-  const int64_t weight_bytes = N * (K / 2) + N * (K / 16);
-  if (N <= 8192 && weight_bytes <= (int64_t(48) << 20)) return 1;
-  const int64_t panel = int64_t(tile_rows) * (K / 2);
-  int64_t g = (int64_t(24) << 20) / (panel > 0 ? panel : 1);
-  if (g < 1) g = 1;
-  if (g > 32) g = 32;
-  return int(g);
-}
-
 // FP4 GEMM + LoRA-up + epilogue reading the prepared workspace.
 h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream) {
   GemmArgs g;
@@ -427,3 +410,22 @@ h3lin_status h3lin_read_status(const void* ws, cudaStream_t stream, int32_t* dev
 }
 
 }  // extern "C"
+
+extern "C" h3lin_status h3lin_merge_lora(const void* w, int64_t N, int64_t K, const float* pre_quant_scale,
+                                         const h3lin_adapter* adapter, float strength, void* w_out,
+                                         cudaStream_t stream) {
+  if (!w || !w_out || !adapter || !adapter->A || !adapter->B) return H3LIN_E_INVALID;
+  if (N < 1 || K < 64 || K % 64 != 0 || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return H3LIN_E_SHAPE;
+  if (!rank_ok(adapter->rank)) return H3LIN_E_SHAPE;
+  if (!std::isfinite(adapter->alpha) || !std::isfinite(strength)) return H3LIN_E_INVALID;
+  if ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(w_out)) & 7u) return H3LIN_E_ALIGN;
+  if (reinterpret_cast<uintptr_t>(pre_quant_scale) & 15u) return H3LIN_E_ALIGN;
+  DeviceInfo d;
+  const h3lin_status s = require_device(&d);
+  if (s != H3LIN_OK) return s;
+  const float c = strength * (adapter->alpha / static_cast<float>(adapter->rank));
+  if (launch_merge_lora(w, adapter->A, adapter->B, pre_quant_scale, w_out, int(N), int(K), adapter->rank, c,
+                        stream) != cudaSuccess)
+    return H3LIN_E_CUDA;
+  return H3LIN_OK;
+}

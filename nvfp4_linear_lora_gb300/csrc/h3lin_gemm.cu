@@ -717,6 +717,23 @@ static cudaError_t launch_dtype(const GemmArgs& a, int sm_count, cudaStream_t st
                 : launch_variant<128, false, false, F32OUT>(a, sm_count, st);
 }
 
+// M-tiles per raster group of the GEMM.  A narrow weight (N <= 8192, packed
+// codes and scales <= 48 MB) stays resident in L2 while its few N tiles are
+// swept, so the raster runs N-fastest and every x panel is read from HBM once
+// (measured on the block: attn-out and down GEMM reads drop from 0.21 and 1.79
+// GB to 0.13 and 0.54 GB).  A wide weight (QKV, gate/up) is evicted by the
+// output streaming through L2 between its reuses; there a group keeps about
+// 24 MB of x panels in L2 while the weight panels pass.
+int raster_group(int64_t N, int64_t K, int tile_rows) {
+  const int64_t weight_bytes = N * (K / 2) + N * (K / 16);
+  if (N <= 8192 && weight_bytes <= (int64_t(48) << 20)) return 1;
+  const int64_t panel = int64_t(tile_rows) * (K / 2);
+  int64_t g = (int64_t(24) << 20) / (panel > 0 ? panel : 1);
+  if (g < 1) g = 1;
+  if (g > 32) g = 32;
+  return int(g);
+}
+
 cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st) {
   if (a.pair) return a.f32out ? launch_pair_dtype<true>(a, sm_count, st) : launch_pair_dtype<false>(a, sm_count, st);
   return a.f32out ? launch_dtype<true>(a, sm_count, st) : launch_dtype<false>(a, sm_count, st);

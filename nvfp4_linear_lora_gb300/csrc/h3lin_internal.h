@@ -58,4 +58,13 @@ struct GemmArgs {
 };
 cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st);
 
+// M-tiles per raster group of the GEMM for a weight [N, K] and tiles of
+// tile_rows rows (h3lin_gemm.cu).
+int raster_group(int64_t N, int64_t K, int tile_rows);
+
+// W'[N, K] = bf16(W + c * (B[N, r] @ A[r, K]) / s[K]) (h3lin_merge.cu; s may be
+// null = 1); in place allowed.
+cudaError_t launch_merge_lora(const void* w, const void* A, const void* B, const float* pqs, void* w_out, int N,
+                              int K, int rank, float c, cudaStream_t stream);
+
 }  // namespace h3lin

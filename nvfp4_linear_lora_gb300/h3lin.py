@@ -67,6 +67,7 @@ _SIGNATURES = {
                                   _vp, _i32, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "h3lin_selftest_wait_timeout": (_i32, [_vp, _sz, _i64, _vp]),
+    "h3lin_merge_lora": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(h3lin_adapter), _f32, _vp, _vp]),
     "h3lin_forward_noalloc": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), _i32,
                                      ctypes.POINTER(h3lin_adapter), _f32, _vp, _i32, _vp]),
 }
@@ -150,6 +151,11 @@ def h3lin_forward_noalloc(x, M, pqs, weight, epilogue, adapter, strength, out, o
     wp = ctypes.byref(weight) if weight is not None else None
     ap = ctypes.byref(adapter) if adapter is not None else None
     return lib().h3lin_forward_noalloc(x, M, pqs, wp, epilogue, ap, strength, out, out_dtype, stream)
+
+
+def h3lin_merge_lora(w, N, K, pqs, adapter, strength, w_out, stream):
+    ap = ctypes.byref(adapter) if adapter is not None else None
+    return lib().h3lin_merge_lora(w, N, K, pqs, ap, strength, w_out, stream)
 
 
 def h3lin_selftest_wait_timeout(ws, ws_bytes, wait_cycles, stream):
@@ -261,6 +267,19 @@ def forward(x, weight, pre_quant_scale=None, adapter=None, strength=1.0, silu_mu
     _check(h3lin_forward(x.data_ptr(), M, _ptr(pre_quant_scale), wc,
                          H3LIN_EPI_SILU_MUL if silu_mul else H3LIN_EPI_NONE, ac, float(strength),
                          out.data_ptr(), code, workspace.data_ptr(), workspace.numel(), _stream()), "h3lin_forward")
+    return out
+
+
+def merge_lora(w, adapter, strength=1.0, pre_quant_scale=None, out=None):
+    """``bf16(w + strength * (alpha/rank) * B @ A / s)`` through ``h3lin_merge_lora``
+    (s = ``pre_quant_scale``, 1 when None); ``out`` may be ``w`` itself (in place)."""
+    torch = _torch()
+    if w.dtype != torch.bfloat16 or w.dim() != 2:
+        raise TypeError("w must be a 2-D bfloat16 tensor")
+    if out is None:
+        out = torch.empty_like(w)
+    _check(h3lin_merge_lora(w.data_ptr(), w.shape[0], w.shape[1], _ptr(pre_quant_scale), adapter.c_struct(),
+                            float(strength), out.data_ptr(), _stream()), "h3lin_merge_lora")
     return out
 
 

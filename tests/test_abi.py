@@ -125,6 +125,25 @@ def test_quantize_rejects_invalid_arguments():
     assert h3lin.h3lin_pack_weight(A, 0, 64, A, A, A, A, 1 << 20, None) == E.H3LIN_E_SHAPE
 
 
+def test_merge_lora_rejects_invalid_arguments():
+    E = h3lin
+    ad = h3lin.h3lin_adapter(A, A, 16, 16.0)
+    m = lambda **kw: h3lin.h3lin_merge_lora(kw.get("w", A), kw.get("N", 384), kw.get("K", 256), kw.get("pqs"),
+                                            kw.get("adapter", ad), kw.get("strength", 1.0), kw.get("out", A), None)
+    assert m(w=None) == E.H3LIN_E_INVALID
+    assert m(out=None) == E.H3LIN_E_INVALID
+    assert m(adapter=None) == E.H3LIN_E_INVALID
+    assert m(adapter=h3lin.h3lin_adapter(A, None, 16, 16.0)) == E.H3LIN_E_INVALID
+    assert m(adapter=h3lin.h3lin_adapter(A, A, 16, math.inf)) == E.H3LIN_E_INVALID
+    assert m(strength=math.nan) == E.H3LIN_E_INVALID
+    assert m(N=0) == E.H3LIN_E_SHAPE
+    assert m(K=96) == E.H3LIN_E_SHAPE
+    assert m(adapter=h3lin.h3lin_adapter(A, A, 24, 24.0)) == E.H3LIN_E_SHAPE
+    assert m(w=A + 4) == E.H3LIN_E_ALIGN
+    assert m(out=A + 2) == E.H3LIN_E_ALIGN
+    assert m(pqs=A + 8) == E.H3LIN_E_ALIGN
+
+
 @pytest.mark.skipif(__import__("tests._util", fromlist=["have_gpu"]).have_gpu(), reason="GPU present")
 def test_valid_call_without_gpu_reports_cuda_error():
     # every host check passes; the call then fails to find a device and says so
