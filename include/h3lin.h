@@ -37,7 +37,11 @@
  *   - Kernels never trap: every device-side wait is bounded; on expiry the
  *     kernel records H3LIN_E_TIMEOUT in the workspace status word and returns.
  *
- * Shape rules: M >= 1; K % 64 == 0; N % 128 == 0 (SiLU*up: N % 256 == 0);
+ * Shape rules: M >= 0; K % 64 == 0; N % 128 == 0 (SiLU*up: N % 256 == 0);
+ * an activation of M = 0 rows is a valid call of h3lin_forward (and its two
+ * stages) or h3lin_quantize_act that enqueues nothing and touches no buffer
+ * (x, out, codes, scales and the workspace may then be NULL); a weight needs
+ * N >= 1;
  * rank % 16 == 0 and 16 <= rank <= 256, or rank % 32 == 0 and rank <= 512;
  * x, codes, scales, out, A, B 16-byte aligned; rows and K below 2^31.
  */

@@ -149,8 +149,9 @@ ForwardLayout forward_layout(int64_t M, int64_t K, int64_t N, int64_t rank) {
 
 h3lin_status quantize_impl(const void* x, int64_t M, int64_t K, const float* pqs, void* codes, void* scales,
                            float* ts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (M < 0 || M > kMaxDim || K < 64 || K > kMaxK || K % 64 != 0) return H3LIN_E_SHAPE;
+  if (M == 0) return H3LIN_OK;   // no rows: nothing to quantise, no buffer touched
   if (!x || !codes || !scales || !ts || !ws) return H3LIN_E_INVALID;
-  if (M < 1 || M > kMaxDim || K < 64 || K > kMaxK || K % 64 != 0) return H3LIN_E_SHAPE;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(ws) || (pqs && !aligned16(pqs)) ||
       (reinterpret_cast<uintptr_t>(ts) & 3u))
     return H3LIN_E_ALIGN;
@@ -186,18 +187,20 @@ struct ForwardCall {
 h3lin_status validate_forward(const void* x, int64_t M, const float* pqs, const h3lin_weight* w, int32_t epilogue,
                               const h3lin_adapter* adapter, float strength, void* out, int32_t out_dtype, void* ws,
                               size_t ws_bytes, bool need_x, bool need_out, ForwardCall* c) {
-  if ((need_x && !x) || !w || (need_out && !out) || !ws) return H3LIN_E_INVALID;
+  const bool empty = M == 0;   // no rows: a valid call that touches no buffer and enqueues nothing
+  if ((!empty && ((need_x && !x) || (need_out && !out) || !ws)) || !w) return H3LIN_E_INVALID;
   if (!w->codes || !w->scales || !w->tensor_scale) return H3LIN_E_INVALID;
   if (epilogue != H3LIN_EPI_NONE && epilogue != H3LIN_EPI_SILU_MUL) return H3LIN_E_INVALID;
   if (out_dtype != H3LIN_OUT_BF16 && out_dtype != H3LIN_OUT_F32) return H3LIN_E_INVALID;
   if (!std::isfinite(strength)) return H3LIN_E_INVALID;
   const int64_t K = w->K, N = w->N;
   const bool silu = epilogue == H3LIN_EPI_SILU_MUL;
-  if (M < 1 || M > kMaxDim || K < 64 || K > kMaxK || K % 64 != 0 || N < 128 || N > kMaxDim || N % 128 != 0)
+  if (M < 0 || M > kMaxDim || K < 64 || K > kMaxK || K % 64 != 0 || N < 128 || N > kMaxDim || N % 128 != 0)
     return H3LIN_E_SHAPE;
   if (silu && N % 256 != 0) return H3LIN_E_SHAPE;
-  if ((need_x && !aligned16(x)) || (need_out && !aligned16(out)) || !aligned16(ws) || !aligned16(w->codes) ||
-      !aligned16(w->scales) || (pqs && !aligned16(pqs)) || (reinterpret_cast<uintptr_t>(w->tensor_scale) & 3u))
+  if ((!empty && ((need_x && !aligned16(x)) || (need_out && !aligned16(out)) || !aligned16(ws))) ||
+      !aligned16(w->codes) || !aligned16(w->scales) || (pqs && !aligned16(pqs)) ||
+      (reinterpret_cast<uintptr_t>(w->tensor_scale) & 3u))
     return H3LIN_E_ALIGN;
   const bool lora = adapter != nullptr && strength != 0.0f;
   int64_t rank = 0;
@@ -208,6 +211,8 @@ h3lin_status validate_forward(const void* x, int64_t M, const float* pqs, const 
     if (!rank_ok(rank)) return H3LIN_E_SHAPE;
     if (!aligned16(adapter->A) || !aligned16(adapter->B)) return H3LIN_E_ALIGN;
   }
+  c->M = M;
+  if (empty) return H3LIN_OK;
   c->L = forward_layout(M, K, N, rank);
   if (ws_bytes < c->L.total) return H3LIN_E_WORKSPACE;
   h3lin_status s = require_device(&c->dev);
@@ -337,7 +342,7 @@ size_t h3lin_scales_bytes(int64_t rows, int64_t K) {
 size_t h3lin_quant_workspace_bytes(void) { return kHeaderBytes; }
 
 size_t h3lin_forward_workspace_bytes(int64_t M, int64_t K, int64_t N, int32_t max_rank) {
-  if (M < 1 || K < 64 || K % 64 != 0 || N < 1 || max_rank < 0) return 0;
+  if (M < 0 || K < 64 || K % 64 != 0 || N < 1 || max_rank < 0) return 0;
   return forward_layout(M, K, N, max_rank).total;
 }
 
@@ -358,6 +363,7 @@ h3lin_status h3lin_quantize_act(const void* x, int64_t M, int64_t K, const float
 
 h3lin_status h3lin_pack_weight(const void* w, int64_t N, int64_t K, void* codes, void* scales, float* tensor_scale,
                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (N < 1) return H3LIN_E_SHAPE;   // a weight has rows (an empty activation is a no-op instead)
   return quantize_impl(w, N, K, nullptr, codes, scales, tensor_scale, ws, ws_bytes, stream);
 }
 
@@ -367,7 +373,7 @@ h3lin_status h3lin_forward(const void* x, int64_t M, const float* pqs, const h3l
   ForwardCall c;
   h3lin_status s = validate_forward(x, M, pqs, w, epilogue, adapter, strength, out, out_dtype, ws, ws_bytes, true,
                                     true, &c);
-  if (s != H3LIN_OK) return s;
+  if (s != H3LIN_OK || c.M == 0) return s;
   s = enqueue_prepare(c, stream);
   if (s != H3LIN_OK) return s;
   return enqueue_gemm(c, stream);
@@ -379,7 +385,7 @@ h3lin_status h3lin_forward_prepare(const void* x, int64_t M, const float* pqs, c
   ForwardCall c;
   h3lin_status s = validate_forward(x, M, pqs, w, H3LIN_EPI_NONE, adapter, strength, nullptr, H3LIN_OUT_BF16, ws,
                                     ws_bytes, true, false, &c);
-  if (s != H3LIN_OK) return s;
+  if (s != H3LIN_OK || c.M == 0) return s;
   return enqueue_prepare(c, stream);
 }
 
@@ -389,7 +395,7 @@ h3lin_status h3lin_forward_gemm(int64_t M, const h3lin_weight* w, int32_t epilog
   ForwardCall c;
   h3lin_status s = validate_forward(nullptr, M, nullptr, w, epilogue, adapter, strength, out, out_dtype, ws,
                                     ws_bytes, false, true, &c);
-  if (s != H3LIN_OK) return s;
+  if (s != H3LIN_OK || c.M == 0) return s;
   return enqueue_gemm(c, stream);
 }
 

@@ -80,7 +80,10 @@ def test_forward_rejects_invalid_arguments():
     assert _fwd(out_dtype=2) == E.H3LIN_E_INVALID
     assert _fwd(strength=math.nan) == E.H3LIN_E_INVALID
     assert _fwd(strength=math.inf) == E.H3LIN_E_INVALID
-    assert _fwd(M=0) == E.H3LIN_E_SHAPE
+    assert _fwd(M=-1) == E.H3LIN_E_SHAPE
+    # no rows: valid, nothing enqueued, no buffer looked at (no device needed)
+    assert _fwd(M=0, x=None, out=None, ws=None) == E.H3LIN_OK
+    assert _fwd(M=0, weight=_weight(384, 200)) == E.H3LIN_E_SHAPE   # other rules still apply
     assert _fwd(weight=_weight(384, 200)) == E.H3LIN_E_SHAPE          # K % 64
     assert _fwd(weight=_weight(300, 256)) == E.H3LIN_E_SHAPE          # N % 128
     assert _fwd(weight=_weight(384, 256), epilogue=1) == E.H3LIN_E_SHAPE  # SiLU needs N % 256
@@ -119,7 +122,8 @@ def test_quantize_rejects_invalid_arguments():
     assert q(x=None) == E.H3LIN_E_INVALID
     assert q(ts=None) == E.H3LIN_E_INVALID
     assert q(K=96) == E.H3LIN_E_SHAPE
-    assert q(M=0) == E.H3LIN_E_SHAPE
+    assert q(M=-1) == E.H3LIN_E_SHAPE
+    assert q(M=0, x=None, codes=None, scales=None, ts=None, ws=None) == E.H3LIN_OK
     assert q(codes=A + 1) == E.H3LIN_E_ALIGN
     assert q(ws_bytes=16) == E.H3LIN_E_WORKSPACE
     assert h3lin.h3lin_pack_weight(A, 0, 64, A, A, A, A, 1 << 20, None) == E.H3LIN_E_SHAPE

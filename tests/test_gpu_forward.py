@@ -161,3 +161,24 @@ def test_device_status_clean():
     ws = h3lin.new_workspace(h3lin.h3lin_forward_workspace_bytes(100, 128, 128, 16))
     h3lin.forward(dev["x"], pw, dev["pqs"], dev["adapter"], 1.0, False, workspace=ws)
     assert h3lin.read_status(ws) == 0
+
+
+def test_empty_input_is_a_no_op():
+    """M = 0 rows: the forward and the quantiser accept it, enqueue nothing and
+    return empty results; a following normal call is unaffected."""
+    K, N, r = 256, 512, 16
+    p = synth.projection(4242, 8, K, N, r)
+    pw = h3lin.pack_weight(synth.to_bf16_tensor(p["W"]).cuda())
+    a = p["adapter"]
+    ad = h3lin.Adapter(synth.to_bf16_tensor(a["A"]).cuda(), synth.to_bf16_tensor(a["B"]).cuda(), r, a["alpha"])
+    s = torch.from_numpy(p["pqs"]).cuda()
+    x0 = torch.empty((0, K), dtype=torch.bfloat16, device="cuda")
+    y0 = h3lin.forward(x0, pw, s, ad, 1.0)
+    assert y0.shape == (0, N)
+    y0s = h3lin.forward(x0, pw, s, ad, 1.0, silu_mul=True)
+    assert y0s.shape == (0, N // 2)
+    codes, scales, ts = h3lin.quantize_act(x0, s)
+    assert codes.numel() == 0
+    torch.cuda.synchronize()
+    got, _, _ = run(p)
+    assert_parity(got, ref(p), "after empty calls")
