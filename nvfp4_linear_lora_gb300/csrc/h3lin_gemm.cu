@@ -524,10 +524,12 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
       const uint32_t smem0 = smem_u32(smem);
       const bool k_full = (K & 255) == 0;
       for (int t = pair; t < num_tiles; t += npairs) {
-        if (!mbar_wait(tmem_empty, acc_ph ^ 1, ab)) goto mma_done;
+        // the tile's first stage is waited for while the epilogue still drains
+        // the accumulator, so the first MMA follows the release directly
+        if (!mbar_wait(&sf_full[st], ph, ab) || !mbar_wait(tmem_empty, acc_ph ^ 1, ab)) goto mma_done;
         tc_fence_after();
         for (int kc = 0; kc < nk; ++kc) {
-          if (!mbar_wait(&sf_full[st], ph, ab)) goto mma_done;
+          if (kc > 0 && !mbar_wait(&sf_full[st], ph, ab)) goto mma_done;
           tc_fence_after();
           const uint32_t a_addr = smem0 + st * C::kStageBytes;
           // +32 bytes along K = +2 in a descriptor's start-address field
