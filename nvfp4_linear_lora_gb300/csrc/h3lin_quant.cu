@@ -58,16 +58,16 @@ struct ColMax8 {
 #pragma unroll
     for (int i = 0; i < 4; ++i) h[i] = __hmax2(h[i], __habs2(*reinterpret_cast<const __nv_bfloat162*>(&u[i])));
   }
-  // max over the 8 columns of |colmax * s|
+  // max over the 8 columns of |colmax * s| (a tree of maxima: short dependency chains)
   __device__ __forceinline__ float scaled_max(const float (&s)[8]) const {
-    float m = 0.0f;
+    float v[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t u = *reinterpret_cast<const uint32_t*>(&h[i]);
-      m = fmaxf(m, __fmul_rn(bf16lo(u), fabsf(s[2 * i])));
-      m = fmaxf(m, __fmul_rn(bf16hi(u), fabsf(s[2 * i + 1])));
+      v[2 * i] = __fmul_rn(bf16lo(u), fabsf(s[2 * i]));
+      v[2 * i + 1] = __fmul_rn(bf16hi(u), fabsf(s[2 * i + 1]));
     }
-    return m;
+    return fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
   }
 };
 
