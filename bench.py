@@ -79,6 +79,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-merged", action="store_true",
                     help="skip the merged-LoRA comparison (weights with the adapter folded in, base path only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU-oracle sample time")
+    ap.add_argument("--unfused-mlp", action="store_true",
+                    help="run gate/up and down as two plain projections (amax pass over h) instead of the "
+                         "MLP's producer fusion")
     return ap.parse_args(argv)
 
 
@@ -118,9 +121,15 @@ def make_block_inputs(S, seed=configs.BLOCK_SEED):
 
 
 class Block:
-    """Device-resident block: packed weights, adapters, workspaces, outputs."""
+    """Device-resident block: packed weights, adapters, workspaces, outputs.
 
-    def __init__(self, host, S, device):
+    With ``fused_mlp`` (the default) gate/up and down run as the MLP's
+    producer fusion: gate/up's epilogue leaves amax(h * s_down) in down's
+    workspace and down's prepare is one pass over h (h3lin_mlp_forward, or its
+    stages when the GEMMs are timed); the results are bit-identical to the
+    unfused chain."""
+
+    def __init__(self, host, S, device, fused_mlp=True):
         import torch
 
         from nvfp4_linear_lora_gb300 import h3lin
@@ -148,10 +157,26 @@ class Block:
             self.proj.append(d)
         # down consumes gate/up's output
         self.proj[3]["x_dev"] = self.proj[2]["out"]
+        self.fused_mlp = fused_mlp
+        if fused_mlp:   # down's workspace also serves h3lin_mlp_forward (both projections)
+            gu, dn = self.proj[2], self.proj[3]
+            wsb = h3lin.h3lin_mlp_workspace_bytes(S, gu["K"], gu["N"], dn["N"], max(gu["rank"], dn["rank"]))
+            dn["ws"] = h3lin.new_workspace(wsb, device)
         torch.cuda.synchronize()
 
     def launches_per_step(self):
-        return 3 * len(self.proj)
+        # per projection: amax (+ A(x)), quantise, GEMM; the fused MLP's down
+        # projection has one pass (quantise + A(h)) instead of two
+        return 3 * len(self.proj) - (1 if self.fused_mlp else 0)
+
+    def _mlp(self):
+        h, gu, dn = self.h3lin, self.proj[2], self.proj[3]
+        st = h.h3lin_mlp_forward(gu["x_dev"].data_ptr(), self.S, gu["pqs_dev"].data_ptr(), gu["wc"], gu["ac"], 1.0,
+                                 dn["pqs_dev"].data_ptr(), dn["wc"], dn["ac"], 1.0, gu["out"].data_ptr(),
+                                 dn["out"].data_ptr(), h.H3LIN_OUT_BF16, dn["ws"].data_ptr(), dn["ws"].numel(),
+                                 dn["stream"])
+        if st:
+            raise h.H3linError(st, "h3lin_mlp_forward")
 
     def step(self, gemm_events=None):
         """One block.  With ``gemm_events`` (list of (start, stop) per
@@ -159,6 +184,11 @@ class Block:
         the GEMM kernel, on the same stream."""
         h = self.h3lin
         for i, d in enumerate(self.proj):
+            fuse = self.fused_mlp and i >= 2
+            if fuse and gemm_events is None:
+                if i == 2:
+                    self._mlp()
+                continue
             if gemm_events is None:
                 st = h.h3lin_forward(d["x_dev"].data_ptr(), self.S, d["pqs_dev"].data_ptr(), d["wc"],
                                      h.H3LIN_EPI_SILU_MUL if d["silu"] else h.H3LIN_EPI_NONE, d["ac"], 1.0,
@@ -167,14 +197,22 @@ class Block:
                 if st:
                     raise h.H3linError(st, "h3lin_forward")
             else:
-                st = h.h3lin_forward_prepare(d["x_dev"].data_ptr(), self.S, d["pqs_dev"].data_ptr(), d["wc"], d["ac"],
-                                             1.0, d["ws"].data_ptr(), d["ws"].numel(), d["stream"])
+                prep = h.h3lin_forward_prepare_produced if (fuse and i == 3) else h.h3lin_forward_prepare
+                st = prep(d["x_dev"].data_ptr(), self.S, d["pqs_dev"].data_ptr(), d["wc"], d["ac"], 1.0,
+                          d["ws"].data_ptr(), d["ws"].numel(), d["stream"])
                 if st:
                     raise h.H3linError(st, "h3lin_forward_prepare")
                 gemm_events[i][0].record()
-                st = h.h3lin_forward_gemm(self.S, d["wc"], h.H3LIN_EPI_SILU_MUL if d["silu"] else h.H3LIN_EPI_NONE,
-                                          d["ac"], 1.0, d["out"].data_ptr(), h.H3LIN_OUT_BF16, d["ws"].data_ptr(),
-                                          d["ws"].numel(), d["stream"])
+                epi = h.H3LIN_EPI_SILU_MUL if d["silu"] else h.H3LIN_EPI_NONE
+                if fuse and i == 2:   # producer: amax of h for down, into down's workspace
+                    nx = self.proj[3]
+                    st = h.h3lin_forward_gemm_produce(self.S, d["wc"], epi, d["ac"], 1.0, d["out"].data_ptr(),
+                                                      d["ws"].data_ptr(), d["ws"].numel(),
+                                                      nx["pqs_dev"].data_ptr(), nx["ws"].data_ptr(),
+                                                      nx["ws"].numel(), d["stream"])
+                else:
+                    st = h.h3lin_forward_gemm(self.S, d["wc"], epi, d["ac"], 1.0, d["out"].data_ptr(),
+                                              h.H3LIN_OUT_BF16, d["ws"].data_ptr(), d["ws"].numel(), d["stream"])
                 if st:
                     raise h.H3linError(st, "h3lin_forward_gemm")
                 gemm_events[i][1].record()
@@ -356,7 +394,7 @@ def native_arm(a, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     S = a.S
     host = make_block_inputs(S)
-    blk = Block(host, S, device)
+    blk = Block(host, S, device, fused_mlp=not a.unfused_mlp)
     peaks, peak_kind = load_peaks()
     total, base, ldown, lup = block_flops(S)
 
@@ -548,6 +586,8 @@ def native_arm(a, rank, world, local_rank):
             "vs_baseline": None, "dtype": "e2m1+bf16", "data": "synthetic",
             "config": {"workload": f"dit_block_4proj_S{S}", "S": S, "hidden": configs.HIDDEN, "mlp": configs.MLP,
                        "ranks": [p[3] for p in configs.BLOCK_PROJECTIONS], "strength": 1.0,
+                       "mlp_path": "producer-fused (gate/up epilogue reduces amax(h*s) for down)" if blk.fused_mlp
+                                   else "unfused (separate amax pass over h)",
                        "l2": f"inputs larger than L2 (each activation >= {S * configs.HIDDEN * 2 / 1e6:.0f} MB), no flush"},
             "ms_per_block": ms, "frac_of_fp4_peak": value / world / peak_fp4,
             "flops_per_block": {"total": total, "base_fp4": base, "lora_down": ldown, "lora_up": lup},

@@ -177,6 +177,67 @@ h3lin_status h3lin_forward_gemm(int64_t M, const h3lin_weight* weight, int32_t e
                                 const h3lin_adapter* adapter, float strength, void* out, int32_t out_dtype,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------- producer fusion */
+/* The MLP's down projection consumes gate/up's SiLU*up output h (MiniMax-H3
+ * Ultra Fast README, "Active optimization stack", row "MLP": fused gate/up,
+ * in-place SiLU*up, NVFP4 down projection).  TURBO.md (h3-blackwell-runtime,
+ * "Implementation") describes the SwiGLU producer packing NVFP4 for the next
+ * projection while it emits the exact BF16 LoRA input.  With a dynamic
+ * per-tensor scale the packing needs amax(h * s_down) over the whole tensor
+ * first, so here the fusion has two phases: the gate/up epilogue reduces the
+ * amax while it stores h, and the down projection's prepare stage then makes
+ * ONE pass over h (quantise + A(h)) instead of two.  Every value is
+ * bit-identical to the unfused chain (h3lin_forward on gate/up, then on down).
+ *
+ * h3lin_forward_gemm_produce: h3lin_forward_gemm with a bf16 output that is
+ * also left, as amax partials, for the consuming projection:
+ *   next_pre_quant_scale  the consumer's pre_quant_scale, device fp32 [N_out] or
+ *                         NULL (N_out = N, or N/2 for SiLU*up); 16-byte aligned
+ *   next_workspace        the consumer's workspace (may be `workspace` itself);
+ *                         its header receives the partials; >= header size
+ *                         (h3lin_quant_workspace_bytes()), 16-byte aligned
+ * The amax is reduced inside the CTA-pair kernel's SiLU*up epilogue; other
+ * shapes get an amax pass over the output instead (same result).
+ *
+ * h3lin_forward_prepare_produced: h3lin_forward_prepare for an x that a
+ * producer GEMM wrote, with the same pre_quant_scale and workspace given to
+ * that producer, on the same stream after it: no amax pass; with an active
+ * adapter a single TMA-staged pass quantises x and computes A(x).  Calling it
+ * without such a producer quantises with stale or zero partials (documented
+ * misuse, not detected). */
+h3lin_status h3lin_forward_gemm_produce(int64_t M, const h3lin_weight* weight, int32_t epilogue,
+                                        const h3lin_adapter* adapter, float strength, void* out,
+                                        void* workspace, size_t workspace_bytes,
+                                        const float* next_pre_quant_scale, void* next_workspace,
+                                        size_t next_workspace_bytes, cudaStream_t stream);
+h3lin_status h3lin_forward_prepare_produced(const void* x, int64_t M, const float* pre_quant_scale,
+                                            const h3lin_weight* weight, const h3lin_adapter* adapter,
+                                            float strength, void* workspace, size_t workspace_bytes,
+                                            cudaStream_t stream);
+
+/* The whole MLP on one stream and one workspace:
+ *   h   = silu(gate(x)) * up(x)   (h3lin_forward with H3LIN_EPI_SILU_MUL, bf16)
+ *   out = down(h)                 (h3lin_forward, out_dtype)
+ * through the producer fusion above.
+ *   x         device bf16 [M, K]
+ *   gate_up   packed [gate; up] weight, N_gu rows (N_gu % 256 == 0), K columns
+ *   down      packed weight with down->K == N_gu / 2
+ *   h         device bf16 [M, N_gu / 2], written (the down projection's input
+ *             and its LoRA input)
+ *   out       device [M, down->N] of out_dtype
+ *   workspace >= h3lin_mlp_workspace_bytes(M, K, N_gu, down->N, max rank)
+ * Each pre_quant_scale / adapter / strength as for h3lin_forward; M == 0 is
+ * a no-op.  Errors are those of h3lin_forward, checked for both projections
+ * before anything is enqueued, plus H3LIN_E_SHAPE when down->K != N_gu / 2. */
+size_t h3lin_mlp_workspace_bytes(int64_t M, int64_t K, int64_t N_gate_up, int64_t N_down, int32_t max_rank);
+h3lin_status h3lin_mlp_forward(const void* x, int64_t M,
+                               const float* gate_up_pre_quant_scale, const h3lin_weight* gate_up,
+                               const h3lin_adapter* gate_up_adapter, float gate_up_strength,
+                               const float* down_pre_quant_scale, const h3lin_weight* down,
+                               const h3lin_adapter* down_adapter, float down_strength,
+                               void* h, void* out, int32_t out_dtype,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------ merged-LoRA weights */
 /* Comparison mode of the dynamic path: the LoRA update folded into the
  * weight before it is packed (MiniMax-H3 Turbo — one file, no Python, "What

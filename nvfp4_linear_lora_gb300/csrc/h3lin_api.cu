@@ -161,9 +161,9 @@ h3lin_status quantize_impl(const void* x, int64_t M, int64_t K, const float* pqs
   if (s != H3LIN_OK) return s;
   float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kPartialsOffset);
   const RowPlan plan = plan_rows(M, K, d.sm_count);
-  if (launch_amax(x, int(M), int(K), pqs, partials, plan, stream) != cudaSuccess) return H3LIN_E_CUDA;
-  if (launch_quant(x, int(M), int(K), pqs, partials, plan.blocks, codes, scales, ts, plan, nullptr, nullptr, 0,
-                   0.0f, nullptr, d.sm_count, stream) != cudaSuccess)
+  if (launch_amax(x, int(M), int(K), pqs, partials, plan, nullptr, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  if (launch_quant(x, int(M), int(K), pqs, partials, plan.blocks, nullptr, codes, scales, ts, plan, nullptr,
+                   nullptr, 0, 0.0f, nullptr, d.sm_count, stream) != cudaSuccess)
     return H3LIN_E_CUDA;
   return H3LIN_OK;
 }
@@ -180,6 +180,14 @@ struct ForwardCall {
   uint8_t* ws;
   ForwardLayout L;
   DeviceInfo dev;
+  bool produced = false;   // prepare: the amax partials were left in ws by a producer GEMM
+};
+
+// Where a producer GEMM leaves the amax of its output for the consuming
+// projection (h3lin_forward_gemm_produce).
+struct Producer {
+  const float* pqs;   // the consumer's pre_quant_scale (null = 1)
+  uint8_t* ws;        // the consumer's workspace
 };
 
 // Host-side validation shared by h3lin_forward and its two stages.  `need_x`
@@ -235,38 +243,53 @@ h3lin_status validate_forward(const void* x, int64_t M, const float* pqs, const 
 }
 
 // amax pass (fused with u = A(x) when the adapter is active) + quantise pass.
+// With c.produced the amax pass is skipped: the partials (and their count)
+// were left in the workspace header by the producer GEMM of x.
 h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
   uint32_t* status = reinterpret_cast<uint32_t*>(c.ws + kStatusOffset);
   float* ts_x = reinterpret_cast<float*>(c.ws + kTsOffset);
   float* partials = reinterpret_cast<float*>(c.ws + kPartialsOffset);
+  const int* produced_count = reinterpret_cast<const int*>(c.ws + kProducedOffset);
   void* xq = c.ws + c.L.codes;
   void* xs = c.ws + c.L.scales;
   void* u = c.ws + c.L.u;
   void* bp = c.ws + c.L.b;
   const RowPlan plan = plan_rows(c.M, c.K, c.dev.sm_count);
   int nparts = plan.blocks;
+  const float lora_k = c.lora ? c.strength * (c.adapter->alpha / float(c.rank)) : 0.0f;
   if (c.lora) {
     CUtensorMap tm_x, tm_a;
     const int a_box = c.rank <= 256 ? int(c.rank) : int(c.rank / 2);
     if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, c.K, c.M, c.K * 2, 64, 128)) return H3LIN_E_CUDA;
     if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.adapter->A, c.K, c.rank, c.K * 2, 64, a_box))
       return H3LIN_E_CUDA;
+    if (c.produced) {   // one pass: quantise + u = A(x) + B'
+      if (launch_quant_lora(tm_x, tm_a, int(c.M), int(c.K), int(c.rank), a_box, c.pqs, partials, produced_count,
+                            xq, xs, ts_x, u, status, c.adapter->B, bp, c.N * c.rank, lora_k, c.w->tensor_scale,
+                            c.dev.sm_count, stream) != cudaSuccess)
+        return H3LIN_E_CUDA;
+      return H3LIN_OK;
+    }
     if (launch_amax_lora(tm_x, tm_a, int(c.M), int(c.K), int(c.rank), a_box, c.pqs, partials, u, status,
                          c.dev.sm_count, &nparts, stream) != cudaSuccess)
       return H3LIN_E_CUDA;
-  } else {
-    if (launch_amax(c.x, int(c.M), int(c.K), c.pqs, partials, plan, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  } else if (!c.produced) {
+    if (launch_amax(c.x, int(c.M), int(c.K), c.pqs, partials, plan, nullptr, stream) != cudaSuccess)
+      return H3LIN_E_CUDA;
   }
-  const float lora_k = c.lora ? c.strength * (c.adapter->alpha / float(c.rank)) : 0.0f;
-  if (launch_quant(c.x, int(c.M), int(c.K), c.pqs, partials, nparts, xq, xs, ts_x, plan,
+  if (launch_quant(c.x, int(c.M), int(c.K), c.pqs, partials, nparts, c.produced ? produced_count : nullptr, xq, xs,
+                   ts_x, plan,
                    c.lora ? c.adapter->B : nullptr, c.lora ? bp : nullptr, c.lora ? c.N * c.rank : 0, lora_k,
                    c.w->tensor_scale, c.dev.sm_count, stream) != cudaSuccess)
     return H3LIN_E_CUDA;
   return H3LIN_OK;
 }
 
-// FP4 GEMM + LoRA-up + epilogue reading the prepared workspace.
-h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream) {
+// FP4 GEMM + LoRA-up + epilogue reading the prepared workspace.  With a
+// producer (bf16 output only) the amax of the output for the consuming
+// projection is left in the producer's workspace: from the pair kernel's
+// SiLU*up epilogue, else by an amax pass over the output.
+h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream, const Producer* prod = nullptr) {
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
   void* xq = c.ws + c.L.codes;
@@ -302,7 +325,19 @@ h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream) {
            make_sf_map(&g.tm_ws, g.ws, size_t(c.N) * size_t(c.K / 16)) &&
            make_out_map(&g.tm_out, c.out, c.f32out, g.ldo, c.M);
   g.group_m = raster_group(c.N, c.K, g.pair ? 256 : 128);
+  const bool fused_amax = prod && g.pair && c.silu && !c.f32out;
+  if (fused_amax) {
+    g.amax_s = prod->pqs;
+    g.amax_out = reinterpret_cast<float*>(prod->ws + kPartialsOffset);
+    g.amax_count = reinterpret_cast<int*>(prod->ws + kProducedOffset);
+  }
   if (launch_fp4gemm(g, c.dev.sm_count, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  if (prod && !fused_amax) {
+    const RowPlan plan = plan_rows(c.M, g.ldo, c.dev.sm_count);
+    if (launch_amax(c.out, int(c.M), g.ldo, prod->pqs, reinterpret_cast<float*>(prod->ws + kPartialsOffset), plan,
+                    reinterpret_cast<int*>(prod->ws + kProducedOffset), stream) != cudaSuccess)
+      return H3LIN_E_CUDA;
+  }
   return H3LIN_OK;
 }
 
@@ -397,6 +432,65 @@ h3lin_status h3lin_forward_gemm(int64_t M, const h3lin_weight* w, int32_t epilog
                                     ws_bytes, false, true, &c);
   if (s != H3LIN_OK || c.M == 0) return s;
   return enqueue_gemm(c, stream);
+}
+
+h3lin_status h3lin_forward_gemm_produce(int64_t M, const h3lin_weight* w, int32_t epilogue,
+                                        const h3lin_adapter* adapter, float strength, void* out, void* ws,
+                                        size_t ws_bytes, const float* next_pqs, void* next_ws, size_t next_ws_bytes,
+                                        cudaStream_t stream) {
+  if (M > 0 && !next_ws) return H3LIN_E_INVALID;
+  if ((next_ws && !aligned16(next_ws)) || (next_pqs && !aligned16(next_pqs))) return H3LIN_E_ALIGN;
+  if (M > 0 && next_ws_bytes < kHeaderBytes) return H3LIN_E_WORKSPACE;
+  ForwardCall c;
+  h3lin_status s = validate_forward(nullptr, M, nullptr, w, epilogue, adapter, strength, out, H3LIN_OUT_BF16, ws,
+                                    ws_bytes, false, true, &c);
+  if (s != H3LIN_OK || c.M == 0) return s;
+  const Producer p{next_pqs, static_cast<uint8_t*>(next_ws)};
+  return enqueue_gemm(c, stream, &p);
+}
+
+h3lin_status h3lin_forward_prepare_produced(const void* x, int64_t M, const float* pqs, const h3lin_weight* w,
+                                            const h3lin_adapter* adapter, float strength, void* ws, size_t ws_bytes,
+                                            cudaStream_t stream) {
+  ForwardCall c;
+  h3lin_status s = validate_forward(x, M, pqs, w, H3LIN_EPI_NONE, adapter, strength, nullptr, H3LIN_OUT_BF16, ws,
+                                    ws_bytes, true, false, &c);
+  if (s != H3LIN_OK || c.M == 0) return s;
+  c.produced = true;
+  return enqueue_prepare(c, stream);
+}
+
+size_t h3lin_mlp_workspace_bytes(int64_t M, int64_t K, int64_t N_gate_up, int64_t N_down, int32_t max_rank) {
+  if (M < 0 || K < 64 || K % 64 != 0 || N_gate_up < 256 || N_gate_up % 256 != 0 || N_down < 1 || max_rank < 0)
+    return 0;
+  const size_t a = forward_layout(M, K, N_gate_up, max_rank).total;
+  const size_t b = forward_layout(M, N_gate_up / 2, N_down, max_rank).total;
+  return a > b ? a : b;
+}
+
+h3lin_status h3lin_mlp_forward(const void* x, int64_t M, const float* gu_pqs, const h3lin_weight* gate_up,
+                               const h3lin_adapter* gu_adapter, float gu_strength, const float* down_pqs,
+                               const h3lin_weight* down, const h3lin_adapter* down_adapter, float down_strength,
+                               void* h, void* out, int32_t out_dtype, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  if (!gate_up || !down) return H3LIN_E_INVALID;
+  if (down->K != gate_up->N / 2) return H3LIN_E_SHAPE;
+  ForwardCall a, b;
+  h3lin_status s = validate_forward(x, M, gu_pqs, gate_up, H3LIN_EPI_SILU_MUL, gu_adapter, gu_strength, h,
+                                    H3LIN_OUT_BF16, ws, ws_bytes, true, true, &a);
+  if (s != H3LIN_OK) return s;
+  s = validate_forward(h, M, down_pqs, down, H3LIN_EPI_NONE, down_adapter, down_strength, out, out_dtype, ws,
+                       ws_bytes, true, true, &b);
+  if (s != H3LIN_OK || M == 0) return s;
+  // one workspace serves both projections: the down stages run after the
+  // gate/up GEMM (stream order), and the producer epilogue writes only the
+  // header's partials while that GEMM reads its own regions
+  b.produced = true;
+  if ((s = enqueue_prepare(a, stream)) != H3LIN_OK) return s;
+  const Producer p{down_pqs, static_cast<uint8_t*>(ws)};
+  if ((s = enqueue_gemm(a, stream, &p)) != H3LIN_OK) return s;
+  if ((s = enqueue_prepare(b, stream)) != H3LIN_OK) return s;
+  return enqueue_gemm(b, stream);
 }
 
 h3lin_status h3lin_read_status(const void* ws, cudaStream_t stream, int32_t* device_status) {

@@ -357,7 +357,7 @@ struct PairCfg {
   static constexpr int kSfCols = 16 + 32;
   static constexpr int kEpiWarps = 16;
   static constexpr int kEpiScratch = 2048;                                          // 32 rows x 64 bytes
-  static constexpr int kSmem = kStages * kStageBytes + kEpiWarps * kEpiScratch + 1024 + 256;
+  static constexpr int kSmem = kStages * kStageBytes + kEpiWarps * kEpiScratch + 1024 + 512;
   static constexpr int kTmemCols = 512;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(256 + kStages * kSfCols <= kTmemCols, "TMEM budget");
@@ -390,14 +390,22 @@ __device__ __forceinline__ void epi_scratch_ready(int lane) {
   __syncwarp();
 }
 
-template <bool SILU, bool LORA, bool F32OUT>
+// AMAX (SiLU*up with a bf16 output only): the epilogue also reduces
+// max |float(h) * s_next| over the tile's valid rows, h the bf16 value it
+// stores and s_next the per-channel pre_quant_scale of the projection that
+// consumes h (null = 1); each CTA writes its maximum to amax_out[blockIdx.x]
+// and CTA 0 the count gridDim.x to *amax_count.  The consumer's quantiser
+// then needs no amax pass over h.
+template <bool SILU, bool LORA, bool F32OUT, bool AMAX>
 __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_wq,
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_b,
     const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_ws,
     const __grid_constant__ CUtensorMap tm_out,
     const float* __restrict__ ts_x, const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K,
-    int rank, int ldo, int group_m, uint32_t* __restrict__ status) {
+    int rank, int ldo, int group_m, uint32_t* __restrict__ status, const float* __restrict__ amax_s,
+    float* __restrict__ amax_out, int* __restrict__ amax_count) {
+  static_assert(!AMAX || (SILU && !F32OUT), "the fused amax serves the bf16 SiLU*up output");
   using C = PairCfg;
   constexpr int kPairCpWarps = PairRoles<SILU>::kCpWarps;
   constexpr int kPairEpiWarp0 = PairRoles<SILU>::kEpiWarp0;
@@ -413,6 +421,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
   uint64_t* drain_cp = drain_bar + 1;   // one per copy warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_cp + kPairCpWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  float* amax_red = reinterpret_cast<float*>(abort_flag + 1);   // one per epilogue warp (AMAX)
 
   const int warp = warp_id(), lane = lane_id();
   const uint32_t crank = cluster_ctarank();
@@ -613,6 +622,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     constexpr int kRoundCols = 64 / kEsize;          // output columns per 64-byte staging row
     constexpr int kRounds = (SILU ? 32 : 64) / kRoundCols;
     uint32_t acc_ph = 0;
+    float am = 0.0f;                         // AMAX: running max of |h * s_next|
     for (int t = pair; t < num_tiles; t += npairs) {
       int tm, tn;
       tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
@@ -647,6 +657,17 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
             w[k] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(lo)), __fmul_rn(scale, __uint_as_float(hi)));
           }
         }
+        if (AMAX && row0 + lane < M) {
+          // per element: |fl(h * s)| with h the stored bf16 value (the lanes'
+          // loads of s are broadcasts: all lanes read the same 32 columns)
+          const int cb = col0 + rd * kRoundCols;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 sv = amax_s ? __ldg(reinterpret_cast<const float2*>(amax_s + cb) + k) : make_float2(1.0f, 1.0f);
+            am = fmaxf(am, fabsf(__fmul_rn(bf16lo(w[k]), sv.x)));
+            am = fmaxf(am, fabsf(__fmul_rn(bf16hi(w[k]), sv.y)));
+          }
+        }
         epi_scratch_ready(lane);
         // row = lane, 64 bytes; 16-byte chunks placed as the 64-byte TMA swizzle expects
 #pragma unroll
@@ -659,9 +680,20 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     }
     if (lane == 0) bulk_wait_group0();   // this warp's output stores are complete
     __syncwarp();
+    if (AMAX) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+      if (lane == 0) amax_red[e] = am;
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (AMAX && threadIdx.x == 0) {
+    float m = amax_red[0];
+    for (int i = 1; i < C::kEpiWarps; ++i) m = fmaxf(m, amax_red[i]);
+    amax_out[blockIdx.x] = m;
+    if (blockIdx.x == 0) *amax_count = static_cast<int>(gridDim.x);
+  }
   cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
@@ -669,9 +701,9 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
   }
 }
 
-template <bool SILU, bool LORA, bool F32OUT>
+template <bool SILU, bool LORA, bool F32OUT, bool AMAX = false>
 static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStream_t st) {
-  auto kern = k_fp4gemm_pair<SILU, LORA, F32OUT>;
+  auto kern = k_fp4gemm_pair<SILU, LORA, F32OUT, AMAX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
   if (e != cudaSuccess) return e;
   const int tiles_m = (a.M + 255) / 256;
@@ -692,11 +724,16 @@ static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStre
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.tm_xs, a.tm_ws, a.tm_out, a.ts_x, a.ts_w,
-                            a.out, a.M, a.N, a.K, a.rank, a.ldo, a.group_m, a.status);
+                            a.out, a.M, a.N, a.K, a.rank, a.ldo, a.group_m, a.status, a.amax_s, a.amax_out,
+                            a.amax_count);
 }
 
 template <bool F32OUT>
 static cudaError_t launch_pair_dtype(const GemmArgs& a, int sm_count, cudaStream_t st) {
+  if (!F32OUT && a.silu && a.amax_out) {
+    return a.lora ? launch_pair_variant<true, true, false, true>(a, sm_count, st)
+                  : launch_pair_variant<true, false, false, true>(a, sm_count, st);
+  }
   if (a.silu) {
     return a.lora ? launch_pair_variant<true, true, F32OUT>(a, sm_count, st)
                   : launch_pair_variant<true, false, F32OUT>(a, sm_count, st);

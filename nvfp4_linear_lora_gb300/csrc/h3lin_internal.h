@@ -11,9 +11,12 @@
 namespace h3lin {
 
 // Workspace header: [0] status word (u32), [4] tensor scale of the last
-// quantised activation (f32), [kPartialsOffset ...] per-CTA amax partials.
+// quantised activation (f32), [8] number of amax partials a producer GEMM left
+// for this workspace's next quantiser (i32), [kPartialsOffset ...] per-CTA
+// amax partials.
 constexpr size_t kStatusOffset = 0;
 constexpr size_t kTsOffset = 4;
+constexpr size_t kProducedOffset = 8;
 constexpr size_t kPartialsOffset = 1024;
 constexpr int kMaxPartials = 4096;
 constexpr size_t kHeaderBytes = kPartialsOffset + kMaxPartials * sizeof(float);  // 17 KB
@@ -29,10 +32,13 @@ struct RowPlan {   // k_amax / k_quant: each thread owns one 16-byte column chun
 RowPlan plan_rows(int64_t M, int64_t K, int sm_count);
 
 // Kernel launchers (enqueue only; arguments already validated).
+// count_out (nullable): block 0 writes the number of partials there.
 cudaError_t launch_amax(const void* x, int M, int K, const float* pqs, float* partials, const RowPlan& p,
-                        cudaStream_t st);
+                        int* count_out, cudaStream_t st);
+// nparts_dev (nullable): the kernel reads the number of partials there instead
+// of taking nparts (partials left by a producer GEMM).
 cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
-                         void* codes, void* scales, float* ts_out, const RowPlan& p,
+                         const int* nparts_dev, void* codes, void* scales, float* ts_out, const RowPlan& p,
                          // optional: B' = bf16(B * lora_k / (ts * ts_w)), elems % 8 == 0
                          const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
                          int sm_count, cudaStream_t st);
@@ -40,6 +46,14 @@ cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const fl
 cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
                              int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
                              int sm_count, int* nparts, cudaStream_t st);
+// The same TMA-staged pass with the amax already known (*nparts_dev partials
+// from a producer GEMM): quantises x * s to codes + native scales and computes
+// u = A(x) in one read of x; writes ts and, like launch_quant, B'.
+cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+                              int a_box_rows, const float* pqs, const float* partials, const int* nparts_dev,
+                              void* codes, void* scales, float* ts_out, void* u, uint32_t* status,
+                              const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
+                              int sm_count, cudaStream_t st);
 // FP4 GEMM + optional LoRA-up + epilogue.
 struct GemmArgs {
   CUtensorMap tm_xq, tm_wq, tm_u, tm_b;
@@ -55,6 +69,11 @@ struct GemmArgs {
   uint32_t* status;
   bool lora, silu, f32out;
   bool pair;                  // use the CTA-pair kernel
+  // producer epilogue (pair kernel, SiLU*up, bf16 output): amax partials of
+  // |h * amax_s| for the consuming projection's quantiser; amax_out null = off
+  const float* amax_s;
+  float* amax_out;
+  int* amax_count;
 };
 cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st);
 

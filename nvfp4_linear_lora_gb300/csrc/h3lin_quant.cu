@@ -10,6 +10,9 @@
 //                E2M1 codes + E4M3 block scales (bit-exact rules below), and
 //                optionally writes B' = B * strength * (alpha/rank) / (ts_x ts_w)
 //                so that the GEMM can accumulate B'(u) into the FP4 tile.
+//   k_amax_lora<QUANT>  when a producer GEMM's epilogue already reduced the
+//                amax of x (the gate/up output feeding down): the TMA-staged
+//                pass quantises x and computes u = A(x) in one read of x.
 //
 // Quantisation rules (float32, round to nearest even at every step):
 //   v = x * s;  ts = amax / 2688 (0 -> 1);  per 16 elements:
@@ -88,7 +91,8 @@ __device__ __forceinline__ float block_max(float m, float* red) {
 // r0 = t / kc (R = rows_step).  The 8 per-channel scales live in registers.
 __global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict__ x, int M, int kc,
                                                        const float* __restrict__ pqs,
-                                                       float* __restrict__ partials, int rows_step) {
+                                                       float* __restrict__ partials, int rows_step,
+                                                       int* __restrict__ count_out) {
   __shared__ float red[kQuantThreads / 32];
   const int tid = blockIdx.x * kQuantThreads + threadIdx.x;
   const int c = tid % kc;
@@ -109,7 +113,10 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict_
     m = cm.scaled_max(s);
   }
   m = block_max(m, red);
-  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+  if (threadIdx.x == 0) {
+    partials[blockIdx.x] = m;
+    if (count_out && blockIdx.x == 0) *count_out = static_cast<int>(gridDim.x);
+  }
 }
 
 // ---------------------------------------------------------------- k_quant
@@ -139,8 +146,9 @@ __device__ __forceinline__ void load_scale16(const float* __restrict__ pqs, int 
 }
 
 // Quantise one 16-element block (two 16-byte halves) of row `row`.
+// The block's codes are stored only when write_codes (rows >= M have none).
 __device__ __forceinline__ void quant_block(const QuantCtx& q, int row, int b, const uint4& w0, const uint4& w1,
-                                            const float (&s)[16], unsigned gmask, int lane) {
+                                            const float (&s)[16], unsigned gmask, int lane, bool write_codes = true) {
   float v[16];
   {
     float h0[8], h1[8], s0[8], s1[8];
@@ -165,7 +173,7 @@ __device__ __forceinline__ void quant_block(const QuantCtx& q, int row, int b, c
   }
   uint2 code = make_uint2(0u, 0u);
   if (isfinite(inv)) code = make_uint2(e2m1x8(qa), e2m1x8(qb));
-  q.codes[static_cast<int64_t>(row) * q.kb + b] = code;
+  if (write_codes) q.codes[static_cast<int64_t>(row) * q.kb + b] = code;
   const uint32_t s1 = __shfl_down_sync(gmask, sb, 1, 4);
   const uint32_t s2 = __shfl_down_sync(gmask, sb, 2, 4);
   const uint32_t s3 = __shfl_down_sync(gmask, sb, 3, 4);
@@ -177,11 +185,12 @@ __device__ __forceinline__ void quant_block(const QuantCtx& q, int row, int b, c
 // in ascending order, so the tail of x is still in L2 when this pass starts.
 __global__ void __launch_bounds__(kQuantThreads) k_quant(
     const uint4* __restrict__ x, int M, int Mpad, int K, const float* __restrict__ pqs,
-    const float* __restrict__ partials, int nparts, uint2* __restrict__ codes, uint8_t* __restrict__ scales,
-    float* __restrict__ ts_out, int rows_step, const uint4* __restrict__ b_src, uint4* __restrict__ b_dst,
-    int64_t b_chunks, float lora_k, const float* __restrict__ ts_w) {
+    const float* __restrict__ partials, int nparts, const int* __restrict__ nparts_dev, uint2* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ ts_out, int rows_step, const uint4* __restrict__ b_src,
+    uint4* __restrict__ b_dst, int64_t b_chunks, float lora_k, const float* __restrict__ ts_w) {
   __shared__ float red[kQuantThreads / 32];
   float m = 0.0f;
+  if (nparts_dev) nparts = min(max(*nparts_dev, 0), kMaxPartials);   // never read past the partials
   for (int i = threadIdx.x; i < nparts; i += kQuantThreads) m = fmaxf(m, partials[i]);
   const float amax = block_max(m, red);
   float ts = __fdiv_rn(amax, 2688.0f);
@@ -254,12 +263,34 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant(
 constexpr int kLoraAmaxWarps = 8;
 constexpr int kLoraRowStride = 32 * kLoraAmaxWarps / 8;   // rows between a thread's rows
 static_assert(128 % kLoraRowStride == 0, "rows of a tile per amax thread");
-constexpr int kLoraThreads = 64 + 32 * kLoraAmaxWarps;
+// The quantising variant does several times the ALU work per byte of the amax
+// pass, so it runs twice the worker warps.
+constexpr int kLoraQuantWarps = 16;
+template <bool QUANT> constexpr int lora_workers() { return QUANT ? kLoraQuantWarps : kLoraAmaxWarps; }
+template <bool QUANT> constexpr int lora_threads() { return 64 + 32 * lora_workers<QUANT>(); }
 
-__global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
+// QUANT: the amax is known (partials_in, *nparts_dev of them, left by a
+// producer GEMM), so warps 2-17 quantise the staged tile instead: thread a
+// owns 16-element block a % 4 of the stage's 64 columns in row a / 4 (the
+// four threads of a row assemble its 32-bit scale word).
+struct QuantPassOut {
+  const float* partials_in;
+  const int* nparts_dev;
+  uint2* codes;
+  uint8_t* scales;
+  float* ts_out;
+  const uint4* b_src;   // optional B' = bf16(B * lora_k / (ts * ts_w)), as k_quant
+  uint4* b_dst;
+  int64_t b_chunks;
+  float lora_k;
+  const float* ts_w;
+};
+
+template <bool QUANT>
+__global__ void __launch_bounds__(lora_threads<QUANT>(), 1) k_amax_lora(
     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a, int M, int K,
     int rank, int a_box_rows, const float* __restrict__ pqs, float* __restrict__ partials,
-    __nv_bfloat16* __restrict__ u, uint32_t* __restrict__ status, int stages, int tmem_cols) {
+    __nv_bfloat16* __restrict__ u, uint32_t* __restrict__ status, int stages, int tmem_cols, QuantPassOut qo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stage_bytes = 16384 + rank * 128;
@@ -272,14 +303,24 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(abort_flag + 1);
 
+  constexpr int kWorkers = lora_workers<QUANT>();
+  constexpr int kThreads = lora_threads<QUANT>();
   const int warp = warp_id(), lane = lane_id();
+  if (QUANT) {   // tensor amax from the producer's partials (every CTA, deterministic)
+    const int n = min(max(*qo.nparts_dev, 0), kMaxPartials);   // never read past the partials
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < n; i += kThreads) m = fmaxf(m, qo.partials_in[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) red[warp] = m;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + kLoraAmaxWarps);
+      mbar_init(&empty[s], 1 + kWorkers);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, kLoraAmaxWarps);
+    mbar_init(tmem_empty, kWorkers);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -297,6 +338,14 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
   const Abort ab{abort_flag, status};
   const int tiles = (M + 127) >> 7;
   const int nk = K >> 6;
+  float ts = 1.0f;
+  if (QUANT) {
+    float m = red[0];
+    for (int i = 1; i < kThreads / 32; ++i) m = fmaxf(m, red[i]);
+    ts = __fdiv_rn(m, 2688.0f);
+    if (ts == 0.0f) ts = 1.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *qo.ts_out = ts;
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -357,23 +406,55 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
   } else {
     // amax + epilogue warps.  TMEM access: warp w reads lanes 32 * (w % 4) ..;
     // the warps of a lane quarter take interleaved 32-column chunks of u.
-    const int aw = warp - 2;                 // 0 .. kLoraAmaxWarps - 1
+    const int aw = warp - 2;                 // 0 .. kWorkers - 1
     const int at = threadIdx.x - 64;         // amax thread
     const int ch = at & 7;                   // 16-byte column chunk
     const int rb = at >> 3;                  // first row
     const int q = warp & 3;
-    const int part = aw >> 2;                // 0 .. kLoraAmaxWarps / 4 - 1
-    constexpr int kParts = kLoraAmaxWarps / 4;
+    const int part = aw >> 2;                // 0 .. kWorkers / 4 - 1
+    constexpr int kParts = kWorkers / 4;
     float m = 0.0f;
     int st = 0;
     uint32_t ph = 0, acc_ph = 0;
+    // QUANT: block qj of rows qr + kQuantRowStep h of each stage; its 16
+    // scales are loaded one stage ahead
+    const int qj = at & 3, qr = at >> 2;
+    const unsigned gmask = 0xFu << (lane & 28);
+    const QuantCtx qc{ts, __fmul_rn(6.0f, ts), K >> 4, K, qo.codes, qo.scales};
+    float qs_next[16];
+    if (QUANT) load_scale16(pqs, qj, qs_next);
     // The per-channel scales of a stage are loaded two stages ahead: the
     // shared-memory ring leaves little L1, so these loads go to L2.
     float s0[8], s1[8];
-    load_scale8(pqs, ch, s0);
-    load_scale8(pqs, (nk > 1 ? 1 : 0) * 8 + ch, s1);
+    if (!QUANT) {
+      load_scale8(pqs, ch, s0);
+      load_scale8(pqs, (nk > 1 ? 1 : 0) * 8 + ch, s1);
+    }
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       for (int kc = 0; kc < nk; ++kc) {
+        if (QUANT) {
+          float qs[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) qs[i] = qs_next[i];
+          const int kn = kc + 1 < nk ? kc + 1 : 0;
+          load_scale16(pqs, 4 * kn + qj, qs_next);
+          if (!mbar_wait(&full[st], ph, ab)) goto amax_done;
+          const uint8_t* tile = smem + st * stage_bytes;
+          constexpr int kQuantRowStep = 8 * kWorkers;   // rows covered by the workers at once
+#pragma unroll
+          for (int h = 0; h < 128 / kQuantRowStep; ++h) {
+            const int r = qr + kQuantRowStep * h;
+            const int row = t * 128 + r;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj) ^ (r & 7)) << 4));
+            const uint4 w1 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj + 1) ^ (r & 7)) << 4));
+            // rows >= M were filled with zeros by the TMA load: scale word 0, no codes
+            quant_block(qc, row, 4 * kc + qj, w0, w1, qs, gmask, lane, row < M);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
+          if (++st == stages) { st = 0; ph ^= 1; }
+          continue;
+        }
         float s[8], s2[8];
         int k2 = kc + 2;
         while (k2 >= nk) k2 -= nk;
@@ -426,14 +507,27 @@ __global__ void __launch_bounds__(kLoraThreads, 1) k_amax_lora(
       if (lane == 0) mbar_arrive(tmem_empty);
       acc_ph ^= 1;
     }
+    if (QUANT && qo.b_chunks > 0) {
+      const float cl = __fdiv_rn(qo.lora_k, __fmul_rn(ts, *qo.ts_w));
+      const int64_t nthreads = static_cast<int64_t>(gridDim.x) * (32 * kWorkers);
+      for (int64_t i = static_cast<int64_t>(blockIdx.x) * (32 * kWorkers) + at; i < qo.b_chunks; i += nthreads) {
+        const uint4 w = __ldg(qo.b_src + i);
+        uint4 o;
+        o.x = pack_bf16x2(__fmul_rn(bf16lo(w.x), cl), __fmul_rn(bf16hi(w.x), cl));
+        o.y = pack_bf16x2(__fmul_rn(bf16lo(w.y), cl), __fmul_rn(bf16hi(w.y), cl));
+        o.z = pack_bf16x2(__fmul_rn(bf16lo(w.z), cl), __fmul_rn(bf16hi(w.z), cl));
+        o.w = pack_bf16x2(__fmul_rn(bf16lo(w.w), cl), __fmul_rn(bf16hi(w.w), cl));
+        qo.b_dst[i] = o;
+      }
+    }
   amax_done:
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) red[aw] = m;
+    if (!QUANT && lane == 0) red[aw] = m;
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (!QUANT && threadIdx.x == 0) {
     float m = red[0];
     for (int i = 1; i < kLoraAmaxWarps; ++i) m = fmaxf(m, red[i]);
     partials[blockIdx.x] = m;
@@ -461,8 +555,9 @@ RowPlan plan_rows(int64_t M, int64_t K, int sm_count) {
 }
 
 cudaError_t launch_amax(const void* x, int M, int K, const float* pqs, float* partials, const RowPlan& p,
-                        cudaStream_t st) {
-  k_amax<<<p.blocks, kQuantThreads, 0, st>>>(static_cast<const uint4*>(x), M, K / 8, pqs, partials, p.rows_step);
+                        int* count_out, cudaStream_t st) {
+  k_amax<<<p.blocks, kQuantThreads, 0, st>>>(static_cast<const uint4*>(x), M, K / 8, pqs, partials, p.rows_step,
+                                             count_out);
   return cudaGetLastError();
 }
 
@@ -489,21 +584,22 @@ static RowPlan plan_quant(int64_t M, int64_t K, int sm_count) {
 }
 
 cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
-                         void* codes, void* scales, float* ts_out, const RowPlan& /*amax plan*/, const void* b_src,
-                         void* b_dst, int64_t b_elems, float lora_k, const float* ts_w, int sm_count,
-                         cudaStream_t st) {
+                         const int* nparts_dev, void* codes, void* scales, float* ts_out, const RowPlan& /*amax plan*/,
+                         const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
+                         int sm_count, cudaStream_t st) {
   const int Mpad = ((M + 127) / 128) * 128;
   const RowPlan p = plan_quant(M, K, sm_count);
   k_quant<<<p.blocks, kQuantThreads, 0, st>>>(
-      static_cast<const uint4*>(x), M, Mpad, K, pqs, partials, nparts, static_cast<uint2*>(codes),
+      static_cast<const uint4*>(x), M, Mpad, K, pqs, partials, nparts, nparts_dev, static_cast<uint2*>(codes),
       static_cast<uint8_t*>(scales), ts_out, p.rows_step, static_cast<const uint4*>(b_src),
       static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w);
   return cudaGetLastError();
 }
 
-cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
-                             int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
-                             int sm_count, int* nparts, cudaStream_t st) {
+template <bool QUANT>
+static cudaError_t launch_lora_pass(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+                                    int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
+                                    int sm_count, const QuantPassOut& qo, int* grid_out, cudaStream_t st) {
   const int stage_bytes = 16384 + rank * 128;
   constexpr int kSmemLimit = 232448;
   int stages = (kSmemLimit - 1024 - 256) / stage_bytes;
@@ -515,12 +611,31 @@ cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, i
   const int tiles = (M + 127) / 128;
   int grid = tiles < sm_count ? tiles : sm_count;
   if (grid > kMaxPartials) grid = kMaxPartials;
-  cudaError_t e = cudaFuncSetAttribute(k_amax_lora, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(k_amax_lora<QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_amax_lora<<<grid, kLoraThreads, smem, st>>>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, partials,
-                                                static_cast<__nv_bfloat16*>(u), status, stages, tmem_cols);
-  *nparts = grid;
+  k_amax_lora<QUANT><<<grid, lora_threads<QUANT>(), smem, st>>>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, partials,
+                                                       static_cast<__nv_bfloat16*>(u), status, stages, tmem_cols, qo);
+  if (grid_out) *grid_out = grid;
   return cudaGetLastError();
+}
+
+cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+                             int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
+                             int sm_count, int* nparts, cudaStream_t st) {
+  QuantPassOut qo{};
+  return launch_lora_pass<false>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, partials, u, status, sm_count, qo, nparts,
+                                 st);
+}
+
+cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+                              int a_box_rows, const float* pqs, const float* partials, const int* nparts_dev,
+                              void* codes, void* scales, float* ts_out, void* u, uint32_t* status,
+                              const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
+                              int sm_count, cudaStream_t st) {
+  QuantPassOut qo{partials, nparts_dev, static_cast<uint2*>(codes), static_cast<uint8_t*>(scales), ts_out,
+                  static_cast<const uint4*>(b_src), static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w};
+  return launch_lora_pass<true>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, nullptr, u, status, sm_count, qo, nullptr,
+                                st);
 }
 
 }  // namespace h3lin

@@ -65,6 +65,14 @@ _SIGNATURES = {
                                      _f32, _vp, _sz, _vp]),
     "h3lin_forward_gemm": (_i32, [_i64, ctypes.POINTER(h3lin_weight), _i32, ctypes.POINTER(h3lin_adapter), _f32,
                                   _vp, _i32, _vp, _sz, _vp]),
+    "h3lin_forward_gemm_produce": (_i32, [_i64, ctypes.POINTER(h3lin_weight), _i32, ctypes.POINTER(h3lin_adapter),
+                                          _f32, _vp, _vp, _sz, _vp, _vp, _sz, _vp]),
+    "h3lin_forward_prepare_produced": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight),
+                                              ctypes.POINTER(h3lin_adapter), _f32, _vp, _sz, _vp]),
+    "h3lin_mlp_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i32]),
+    "h3lin_mlp_forward": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter), _f32,
+                                 _vp, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter), _f32,
+                                 _vp, _vp, _i32, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "h3lin_selftest_wait_timeout": (_i32, [_vp, _sz, _i64, _vp]),
     "h3lin_merge_lora": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(h3lin_adapter), _f32, _vp, _vp]),
@@ -143,6 +151,32 @@ def h3lin_forward_gemm(M, weight, epilogue, adapter, strength, out, out_dtype, w
     wp = ctypes.byref(weight) if weight is not None else None
     ap = ctypes.byref(adapter) if adapter is not None else None
     return lib().h3lin_forward_gemm(M, wp, epilogue, ap, strength, out, out_dtype, ws, ws_bytes, stream)
+
+
+def _ref(s):
+    return ctypes.byref(s) if s is not None else None
+
+
+def h3lin_forward_gemm_produce(M, weight, epilogue, adapter, strength, out, ws, ws_bytes, next_pqs, next_ws,
+                               next_ws_bytes, stream):
+    return lib().h3lin_forward_gemm_produce(M, _ref(weight), epilogue, _ref(adapter), strength, out, ws, ws_bytes,
+                                            next_pqs, next_ws, next_ws_bytes, stream)
+
+
+def h3lin_forward_prepare_produced(x, M, pqs, weight, adapter, strength, ws, ws_bytes, stream):
+    return lib().h3lin_forward_prepare_produced(x, M, pqs, _ref(weight), _ref(adapter), strength, ws, ws_bytes,
+                                                stream)
+
+
+def h3lin_mlp_workspace_bytes(M, K, N_gate_up, N_down, max_rank):
+    return lib().h3lin_mlp_workspace_bytes(M, K, N_gate_up, N_down, max_rank)
+
+
+def h3lin_mlp_forward(x, M, gu_pqs, gate_up, gu_adapter, gu_strength, down_pqs, down, down_adapter, down_strength,
+                      h, out, out_dtype, ws, ws_bytes, stream):
+    return lib().h3lin_mlp_forward(x, M, gu_pqs, _ref(gate_up), _ref(gu_adapter), gu_strength, down_pqs,
+                                   _ref(down), _ref(down_adapter), down_strength, h, out, out_dtype, ws, ws_bytes,
+                                   stream)
 
 
 def h3lin_forward_noalloc(x, M, pqs, weight, epilogue, adapter, strength, out, out_dtype, stream):
@@ -268,6 +302,33 @@ def forward(x, weight, pre_quant_scale=None, adapter=None, strength=1.0, silu_mu
                          H3LIN_EPI_SILU_MUL if silu_mul else H3LIN_EPI_NONE, ac, float(strength),
                          out.data_ptr(), code, workspace.data_ptr(), workspace.numel(), _stream()), "h3lin_forward")
     return out
+
+
+def mlp_forward(x, gate_up, down, gate_up_pre_quant_scale=None, down_pre_quant_scale=None, gate_up_adapter=None,
+                down_adapter=None, gate_up_strength=1.0, down_strength=1.0, h=None, out=None, out_dtype=None,
+                workspace=None):
+    """The MLP ``down(silu(gate(x)) * up(x))`` through ``h3lin_mlp_forward``
+    (producer fusion: gate/up's epilogue reduces the amax of h for down's
+    quantiser).  Returns ``(h, out)``; h is bf16 [M, N_gu/2]."""
+    torch = _torch()
+    M = x.shape[0]
+    if h is None:
+        h = torch.empty((M, gate_up.N // 2), dtype=torch.bfloat16, device=x.device)
+    if out is None:
+        out = torch.empty((M, down.N), dtype=out_dtype or torch.bfloat16, device=x.device)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    code = H3LIN_OUT_F32 if out.dtype == torch.float32 else H3LIN_OUT_BF16
+    if workspace is None:
+        r = max(gate_up_adapter.rank if gate_up_adapter else 0, down_adapter.rank if down_adapter else 0)
+        workspace = new_workspace(h3lin_mlp_workspace_bytes(M, gate_up.K, gate_up.N, down.N, r), x.device)
+    _check(h3lin_mlp_forward(x.data_ptr(), M, _ptr(gate_up_pre_quant_scale), gate_up.c_struct(),
+                             gate_up_adapter.c_struct() if gate_up_adapter else None, float(gate_up_strength),
+                             _ptr(down_pre_quant_scale), down.c_struct(),
+                             down_adapter.c_struct() if down_adapter else None, float(down_strength),
+                             h.data_ptr(), out.data_ptr(), code, workspace.data_ptr(), workspace.numel(),
+                             _stream()), "h3lin_mlp_forward")
+    return h, out
 
 
 def merge_lora(w, adapter, strength=1.0, pre_quant_scale=None, out=None):

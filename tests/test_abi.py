@@ -148,6 +148,49 @@ def test_merge_lora_rejects_invalid_arguments():
     assert m(pqs=A + 8) == E.H3LIN_E_ALIGN
 
 
+def test_mlp_and_producer_argument_checks():
+    E = h3lin
+    gu, dn = _weight(1024, 256), _weight(384, 512)
+
+    def mlp(**kw):
+        a = dict(x=A, M=200, gu=gu, dn=dn, h=A, out=A, ws=A, ws_bytes=1 << 30)
+        a.update(kw)
+        return h3lin.h3lin_mlp_forward(a["x"], a["M"], None, a["gu"], None, 1.0, None, a["dn"], None, 1.0, a["h"],
+                                       a["out"], 0, a["ws"], a["ws_bytes"], None)
+
+    assert mlp(gu=None) == E.H3LIN_E_INVALID
+    assert mlp(dn=_weight(384, 256)) == E.H3LIN_E_SHAPE       # down's K must be N_gate_up / 2
+    assert mlp(M=-1) == E.H3LIN_E_SHAPE
+    assert mlp(h=None) == E.H3LIN_E_INVALID
+    assert mlp(h=A + 4) == E.H3LIN_E_ALIGN
+    assert mlp(ws_bytes=4096) == E.H3LIN_E_WORKSPACE
+    assert mlp(M=0, x=None, h=None, out=None, ws=None) == E.H3LIN_OK
+    assert mlp(gu=_weight(1152, 256), dn=_weight(384, 576)) == E.H3LIN_E_SHAPE   # SiLU*up needs N % 256
+
+    def produce(**kw):
+        a = dict(M=200, w=gu, out=A, ws=A, ws_bytes=1 << 30, next_pqs=None, next_ws=A, next_bytes=1 << 20)
+        a.update(kw)
+        return h3lin.h3lin_forward_gemm_produce(a["M"], a["w"], 1, None, 1.0, a["out"], a["ws"], a["ws_bytes"],
+                                                a["next_pqs"], a["next_ws"], a["next_bytes"], None)
+
+    assert produce(next_ws=None) == E.H3LIN_E_INVALID
+    assert produce(next_ws=A + 8) == E.H3LIN_E_ALIGN
+    assert produce(next_pqs=A + 4) == E.H3LIN_E_ALIGN
+    assert produce(next_bytes=64) == E.H3LIN_E_WORKSPACE
+    assert produce(M=0, out=None, ws=None, next_ws=None) == E.H3LIN_OK
+    assert produce(M=-3) == E.H3LIN_E_SHAPE
+    assert h3lin.h3lin_forward_prepare_produced(A, -1, None, dn, None, 1.0, A, 1 << 30, None) == E.H3LIN_E_SHAPE
+    assert h3lin.h3lin_forward_prepare_produced(None, 5, None, dn, None, 1.0, A, 1 << 30, None) == E.H3LIN_E_INVALID
+
+
+def test_mlp_workspace_is_the_larger_projection_workspace():
+    M, K, Ngu, Nd, r = 37726, 5120, 27648, 5120, 128
+    want = max(h3lin.h3lin_forward_workspace_bytes(M, K, Ngu, r), h3lin.h3lin_forward_workspace_bytes(M, Ngu // 2, Nd, r))
+    assert h3lin.h3lin_mlp_workspace_bytes(M, K, Ngu, Nd, r) == want
+    assert h3lin.h3lin_mlp_workspace_bytes(M, K, 1000, Nd, r) == 0      # gate/up rows % 256
+    assert h3lin.h3lin_mlp_workspace_bytes(-1, K, Ngu, Nd, r) == 0
+
+
 @pytest.mark.skipif(__import__("tests._util", fromlist=["have_gpu"]).have_gpu(), reason="GPU present")
 def test_valid_call_without_gpu_reports_cuda_error():
     # every host check passes; the call then fails to find a device and says so

@@ -1,0 +1,217 @@
+"""Producer fusion for the MLP's down projection on the GPU.
+
+The gate/up GEMM's epilogue reduces amax(h * s_down) while it stores h, and
+the down projection's prepare stage makes one pass over h (quantise + A(h)).
+Max is exact and A(h) runs the same MMA sequence, so every value must be
+bit-identical to the unfused chain (h3lin_forward on gate/up, then on down);
+h and the down output are also checked against the oracle at the parity bar
+(h on the fp32 output mode, of which the stored bf16 h must be the exact
+rounding, as for every projection; the down output against the oracle's down
+applied to the GPU's own bf16 h)."""
+import numpy as np
+import pytest
+
+from tests._util import assert_parity, have_gpu
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not have_gpu(), reason="needs a CUDA GPU")]
+
+torch = pytest.importorskip("torch")
+
+from nvfp4_linear_lora_gb300 import build as h3build  # noqa: E402
+from nvfp4_linear_lora_gb300 import configs, h3lin, synth  # noqa: E402
+from oracle import linear  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    h3build.build()
+
+
+def _dev_adapter(a):
+    if a is None:
+        return None
+    return h3lin.Adapter(synth.to_bf16_tensor(a["A"]).cuda(), synth.to_bf16_tensor(a["B"]).cuda(), a["rank"],
+                         a["alpha"])
+
+
+class Mlp:
+    """gate/up [Ngu, K] (SiLU*up) feeding down [Nd, Ngu/2], host and device copies."""
+
+    def __init__(self, seed, M, K, Ngu, Nd, r_gu, r_d, with_pqs=True):
+        rng = np.random.default_rng(seed)
+        H = Ngu // 2
+        self.x = synth.activation(rng, M, K)
+        self.s_gu = synth.pre_quant_scale(rng, K) if with_pqs else None
+        self.s_d = synth.pre_quant_scale(rng, H) if with_pqs else None
+        self.W_gu = synth.weight(rng, Ngu, K)
+        self.W_d = synth.weight(rng, Nd, H)
+        self.a_gu = synth.adapter(rng, Ngu, K, r_gu) if r_gu else None
+        self.a_d = synth.adapter(rng, Nd, H, r_d) if r_d else None
+        self.xd = synth.to_bf16_tensor(self.x).cuda()
+        self.sd_gu = torch.from_numpy(self.s_gu).cuda() if with_pqs else None
+        self.sd_d = torch.from_numpy(self.s_d).cuda() if with_pqs else None
+        self.pw_gu = h3lin.pack_weight(synth.to_bf16_tensor(self.W_gu).cuda())
+        self.pw_d = h3lin.pack_weight(synth.to_bf16_tensor(self.W_d).cuda())
+        self.ad_gu = _dev_adapter(self.a_gu)
+        self.ad_d = _dev_adapter(self.a_d)
+
+    def fused(self, out_dtype=torch.bfloat16, s_gu=1.0, s_d=1.0):
+        M = self.x.shape[0]
+        r = max(self.ad_gu.rank if self.ad_gu else 0, self.ad_d.rank if self.ad_d else 0)
+        ws = h3lin.new_workspace(h3lin.h3lin_mlp_workspace_bytes(M, self.pw_gu.K, self.pw_gu.N, self.pw_d.N, r))
+        h, y = h3lin.mlp_forward(self.xd, self.pw_gu, self.pw_d, self.sd_gu, self.sd_d, self.ad_gu, self.ad_d, s_gu,
+                                 s_d, out_dtype=out_dtype, workspace=ws)
+        torch.cuda.synchronize()
+        assert h3lin.read_status(ws) == 0
+        return h, y
+
+    def chain(self, out_dtype=torch.bfloat16, s_gu=1.0, s_d=1.0):
+        h = h3lin.forward(self.xd, self.pw_gu, self.sd_gu, self.ad_gu, s_gu, True)
+        y = h3lin.forward(h, self.pw_d, self.sd_d, self.ad_d, s_d, False, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        return h, y
+
+
+MLP_CASES = [
+    # seed, M, K, Ngu, Nd, r_gu, r_d, pqs
+    (1, 300, 1024, 2560, 1024, 128, 64, True),
+    (2, 257, 512, 1024, 640, 64, 0, True),       # down N % 256 != 0 (1-CTA GEMM), base-only down
+    (3, 129, 256, 512, 256, 0, 128, False),      # base-only gate/up, adapter on down, no pre_quant_scale
+    (4, 1000, 768, 1536, 512, 0, 0, True),       # base-only both: produced k_quant path
+    (5, 1, 512, 768 * 2, 384, 32, 16, True),     # a single row
+]
+
+
+@pytest.mark.parametrize("seed,M,K,Ngu,Nd,r_gu,r_d,pqs", MLP_CASES)
+def test_mlp_bitwise_equals_unfused_chain(seed, M, K, Ngu, Nd, r_gu, r_d, pqs):
+    m = Mlp(seed, M, K, Ngu, Nd, r_gu, r_d, pqs)
+    for dt in (torch.bfloat16, torch.float32):
+        hf, yf = m.fused(dt)
+        hc, yc = m.chain(dt)
+        assert torch.equal(hf.view(torch.int16), hc.view(torch.int16)), "h"
+        assert torch.equal(yf.view(torch.int16) if dt == torch.bfloat16 else yf.view(torch.int32),
+                           yc.view(torch.int16) if dt == torch.bfloat16 else yc.view(torch.int32)), f"out {dt}"
+
+
+@pytest.mark.parametrize("seed,M,K,Ngu,Nd,r_gu,r_d,pqs", MLP_CASES[:3])
+def test_mlp_matches_oracle(seed, M, K, Ngu, Nd, r_gu, r_d, pqs):
+    m = Mlp(seed, M, K, Ngu, Nd, r_gu, r_d, pqs)
+    h, y = m.fused(torch.float32)
+    h32 = h3lin.forward(m.xd, m.pw_gu, m.sd_gu, m.ad_gu, 1.0, True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(h, h32.to(torch.bfloat16)), "stored h is not the rounding of the fp32 gate/up output"
+    ref_h = linear.forward(m.x, linear.pack_weight(m.W_gu), m.s_gu, m.a_gu, 1.0, True)
+    assert_parity(h32.cpu().numpy(), ref_h, "h (fp32 mode) vs oracle gate/up")
+    h_host = h.float().cpu().numpy()
+    ref_y = linear.forward(h_host, linear.pack_weight(m.W_d), m.s_d, m.a_d, 1.0, False)
+    assert_parity(y.cpu().numpy(), ref_y, "down(h) vs oracle")
+
+
+def test_mlp_strengths_and_disabled_down():
+    m = Mlp(11, 384, 512, 1024, 512, 64, 64, True)
+    for s_gu, s_d in ((0.5, 2.0), (1.0, 0.0), (0.0, 1.0)):
+        hf, yf = m.fused(torch.bfloat16, s_gu, s_d)
+        hc, yc = m.chain(torch.bfloat16, s_gu, s_d)
+        assert torch.equal(hf.view(torch.int16), hc.view(torch.int16))
+        assert torch.equal(yf.view(torch.int16), yc.view(torch.int16))
+
+
+def test_mlp_empty_is_a_no_op():
+    m = Mlp(12, 8, 256, 512, 256, 16, 16, True)
+    x0 = m.xd[:0]
+    h = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    ws = h3lin.new_workspace(h3lin.h3lin_quant_workspace_bytes())
+    h3lin.mlp_forward(x0, m.pw_gu, m.pw_d, m.sd_gu, m.sd_d, m.ad_gu, m.ad_d, h=h, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert h3lin.read_status(ws) == 0
+
+
+def _stage_produce(src_x, pw, s_in, ad, silu, out, ws, next_s, next_ws):
+    st = h3lin._stream()
+    M = src_x.shape[0]
+    h3lin._check(h3lin.h3lin_forward_prepare(src_x.data_ptr(), M, h3lin._ptr(s_in), pw.c_struct(),
+                                             ad.c_struct() if ad else None, 1.0, ws.data_ptr(), ws.numel(), st),
+                 "prepare")
+    h3lin._check(h3lin.h3lin_forward_gemm_produce(M, pw.c_struct(),
+                                                  h3lin.H3LIN_EPI_SILU_MUL if silu else h3lin.H3LIN_EPI_NONE,
+                                                  ad.c_struct() if ad else None, 1.0, out.data_ptr(), ws.data_ptr(),
+                                                  ws.numel(), h3lin._ptr(next_s), next_ws.data_ptr(),
+                                                  next_ws.numel(), st), "gemm_produce")
+
+
+def _stage_consume(x, pw, s, ad, out, ws):
+    st = h3lin._stream()
+    M = x.shape[0]
+    h3lin._check(h3lin.h3lin_forward_prepare_produced(x.data_ptr(), M, h3lin._ptr(s), pw.c_struct(),
+                                                      ad.c_struct() if ad else None, 1.0, ws.data_ptr(), ws.numel(),
+                                                      st), "prepare_produced")
+    h3lin._check(h3lin.h3lin_forward_gemm(M, pw.c_struct(), h3lin.H3LIN_EPI_NONE, ad.c_struct() if ad else None, 1.0,
+                                          out.data_ptr(), h3lin.H3LIN_OUT_BF16, ws.data_ptr(), ws.numel(), st),
+                 "gemm")
+
+
+@pytest.mark.parametrize("silu", [True, False])
+def test_stage_api_separate_workspaces(silu):
+    """gemm_produce into another projection's workspace, then prepare_produced
+    there; the non-SiLU producer takes the amax pass over its output."""
+    rng = np.random.default_rng(21)
+    M, K, N1 = 333, 512, 1024
+    K2 = N1 // 2 if silu else N1
+    N2 = 768
+    x = synth.activation(rng, M, K)
+    W1, W2 = synth.weight(rng, N1, K), synth.weight(rng, N2, K2)
+    s1, s2 = synth.pre_quant_scale(rng, K), synth.pre_quant_scale(rng, K2)
+    a1, a2 = _dev_adapter(synth.adapter(rng, N1, K, 64)), _dev_adapter(synth.adapter(rng, N2, K2, 128))
+    xd = synth.to_bf16_tensor(x).cuda()
+    pw1, pw2 = h3lin.pack_weight(synth.to_bf16_tensor(W1).cuda()), h3lin.pack_weight(synth.to_bf16_tensor(W2).cuda())
+    sd1, sd2 = torch.from_numpy(s1).cuda(), torch.from_numpy(s2).cuda()
+    ws1 = h3lin.new_workspace(h3lin.h3lin_forward_workspace_bytes(M, K, N1, 64))
+    ws2 = h3lin.new_workspace(h3lin.h3lin_forward_workspace_bytes(M, K2, N2, 128))
+    mid = torch.empty((M, K2), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
+    _stage_produce(xd, pw1, sd1, a1, silu, mid, ws1, sd2, ws2)
+    _stage_consume(mid, pw2, sd2, a2, y, ws2)
+    torch.cuda.synchronize()
+    assert h3lin.read_status(ws1) == 0 and h3lin.read_status(ws2) == 0
+    mid_c = h3lin.forward(xd, pw1, sd1, a1, 1.0, silu)
+    y_c = h3lin.forward(mid_c, pw2, sd2, a2, 1.0, False)
+    torch.cuda.synchronize()
+    assert torch.equal(mid.view(torch.int16), mid_c.view(torch.int16))
+    assert torch.equal(y.view(torch.int16), y_c.view(torch.int16))
+
+
+def test_mlp_block_S37726_bitwise_and_sampled_parity():
+    """The block's gate/up -> down at full size, in the benchmark's
+    configuration: fused equals the unfused chain bit for bit, and sampled
+    rows of both outputs meet the parity bar against the oracle."""
+    S = configs.BLOCK_S
+    proj = {p[0]: p for p in configs.BLOCK_PROJECTIONS}
+    _, K, Ngu, r_gu, _ = proj["gate_up"]
+    _, H, Nd, r_d, _ = proj["down"]
+    assert H == Ngu // 2
+    m = Mlp(configs.BLOCK_SEED + 7, S, K, Ngu, Nd, r_gu, r_d, True)
+    hf, yf = m.fused(torch.bfloat16)
+    hc, yc = m.chain(torch.bfloat16)
+    assert torch.equal(hf.view(torch.int16), hc.view(torch.int16))
+    assert torch.equal(yf.view(torch.int16), yc.view(torch.int16))
+    del hc, yc
+    rng = np.random.default_rng(5)
+    rows = np.array(sorted(set(rng.choice(S, 256, replace=False).tolist()) | set(range((S - 1) // 128 * 128, S))))
+    idx = torch.from_numpy(rows).cuda()
+    # h on sampled rows against the oracle (tensor scale over all of x), on the
+    # fp32 output mode; the stored bf16 h is its rounding
+    from oracle import nvfp4
+    h32 = h3lin.forward(m.xd, m.pw_gu, m.sd_gu, m.ad_gu, 1.0, True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(hf, h32.to(torch.bfloat16))
+    amax_x = nvfp4.tensor_amax_chunked(m.x, m.s_gu)
+    ref_h = linear.forward(m.x, linear.pack_weight(m.W_gu), m.s_gu, m.a_gu, 1.0, True, rows=rows, x_amax=amax_x)
+    assert_parity(h32.index_select(0, idx).cpu().numpy(), ref_h, "block h")
+    del h32
+    # down on sampled rows, from the GPU's whole h (its tensor scale spans all rows)
+    h_host = hf.float().cpu().numpy()
+    amax_h = nvfp4.tensor_amax_chunked(h_host, m.s_d)
+    _, yf32 = m.fused(torch.float32)
+    ref_y = linear.forward(h_host, linear.pack_weight(m.W_d), m.s_d, m.a_d, 1.0, False, rows=rows, x_amax=amax_h)
+    assert_parity(yf32.index_select(0, idx).cpu().numpy(), ref_y, "block down")
