@@ -36,9 +36,9 @@ from nvfp4_linear_lora_gb300 import configs, synth  # noqa: E402
 # profiles/dram_fp4gemm_pair_S37726.md.  It is reported only while the GEMM
 # sources hash to the value the capture was taken with; after any change to
 # them the counters no longer describe the kernel and `traffic` is null.
-GEMM_TRAFFIC = {"sources_sha256": "aca5abb52ab9b1f76f6cf552efcf79e04b25552bc8ac6b4e59db41525157d26c", "S": 37726,
-                "bytes_per_launch": {"qkv": 519622912 + 1120142080, "attn_out": 135361024 + 338501376,
-                                     "gate_up": 577948672 + 1008096768, "down": 550391040 + 367263744}}
+GEMM_TRAFFIC = {"sources_sha256": "2d6443229f9444a0a1d1f0f5a80c6a7f1b8dfc3a3cd770c9f94306580b14982c", "S": 37726,
+                "bytes_per_launch": {"qkv": 509207040 + 1118639616, "attn_out": 135006720 + 338439424,
+                                     "gate_up": 558959104 + 1007155968, "down": 560922112 + 368015872}}
 GEMM_SOURCES = ("nvfp4_linear_lora_gb300/csrc/h3lin_gemm.cu", "nvfp4_linear_lora_gb300/csrc/h3lin_device.cuh")
 
 
