@@ -31,6 +31,15 @@ SWITCH_SEED = 4
 SWITCH_ADAPTER_SEEDS = (41, 42)
 SWITCH_STRENGTHS = (0.0, 0.5, 1.0)
 SWEEP_M = (1024, 4096, 16384, 37726, 65536)
+
+# Q/K RMSNorm + partial split-half three-axis RoPE after the QKV projection:
+# 40 heads of 128 (hidden 5120), 96 rotated dimensions (MiniMax-H3 Turbo — one
+# file, no Python, list of conventions before "Two clocks"), split equally over
+# (t, h, w); positions of a 768 x 1344 canvas in 16-pixel patches (48 x 84 per
+# frame) over 9 frames, the rest of the packed rows along t.
+ROPE = dict(heads=HIDDEN // 128, head_dim=128, rot=96, axis_dims=(32, 32, 32), theta=10000.0, eps=1e-6,
+            frames=9, height=48, width=84)
+ROPE_SEED = 8
 SWEEP_SEEDS = (3, 4, 5, 6, 7)
 
 

@@ -12,7 +12,9 @@ Value laws (one per workload, see ``configs.py``):
   channels (a seeded permutation) multiplied by 20 ("outlier channels");
 * ``pre_quant_scale``: U(0.5, 2) per input channel, float32;
 * base weight ``W``: N(0, 1/K), rounded to bf16 before NVFP4 packing;
-* LoRA ``A [r, K]``: N(0, 1/K); ``B [N, r]``: 0.1 * N(0, 1/r); both bf16.
+* LoRA ``A [r, K]``: N(0, 1/K); ``B [N, r]``: 0.1 * N(0, 1/r); both bf16;
+* Q/K RMSNorm gains: 1 + 0.1 * N(0, 1); RoPE positions: integer video-grid
+  coordinates (``rope_positions``), no randomness.
 
 Draw order inside one generator: x, outlier channel indices, s, W, A, B.
 """
@@ -80,6 +82,23 @@ def adapter(rng, N, K, rank, alpha=None):
     A = bf16_round(_normal(rng, (rank, K), std=1.0 / np.sqrt(K)))
     B = bf16_round(_normal(rng, (N, rank), std=0.1 / np.sqrt(rank)))
     return {"A": A, "B": B, "rank": int(rank), "alpha": float(rank if alpha is None else alpha)}
+
+
+def norm_gain(rng, D):
+    """RMSNorm gain: 1 + 0.1 * N(0, 1) per dimension, float32."""
+    return (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+
+
+def rope_positions(M, frames, height, width):
+    """Integer (t, h, w) position of every packed row, int32 [M, 3]: a t-major
+    frames x height x width video grid first, then the remaining rows along
+    t only (t = frames, frames + 1, ...; h = w = 0)."""
+    r = np.arange(M, dtype=np.int64)
+    grid = frames * height * width
+    t = np.where(r < grid, r // (height * width), frames + (r - grid))
+    h = np.where(r < grid, (r // width) % height, 0)
+    w = np.where(r < grid, r % width, 0)
+    return np.stack([t, h, w], axis=1).astype(np.int32)
 
 
 def projection(seed, M, K, N, rank, law="normal", outlier_frac=0.0, with_adapter=True,
