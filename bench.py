@@ -79,6 +79,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-merged", action="store_true",
                     help="skip the merged-LoRA comparison (weights with the adapter folded in, base path only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU-oracle sample time")
+    ap.add_argument("--no-rope", action="store_true",
+                    help="skip the Q/K RMSNorm + RoPE measurement on the block's QKV output")
     ap.add_argument("--unfused-mlp", action="store_true",
                     help="run gate/up and down as two plain projections (amax pass over h) instead of the "
                          "MLP's producer fusion")
@@ -433,6 +435,44 @@ def native_arm(a, rank, world, local_rank):
         ms = float(t.item())
     value = world * total / (ms * 1e-3) / 1e12
 
+    # the step after QKV: Q/K RMSNorm + split-half three-axis RoPE, in place on
+    # the block's QKV output (1.16 GB, larger than L2), timed alone
+    rope_line = None
+    if not a.no_rope:
+        c = configs.ROPE
+        qkv_out = blk.proj[0]["out"]
+        rrng = np.random.default_rng(configs.ROPE_SEED)
+        wq = torch.from_numpy(synth.norm_gain(rrng, 128)).to(device)
+        wk = torch.from_numpy(synth.norm_gain(rrng, 128)).to(device)
+        pos = torch.from_numpy(synth.rope_positions(S, c["frames"], c["height"], c["width"])).to(device)
+        h3r = blk.h3lin
+        ws_r = h3r.new_workspace(h3r.h3lin_quant_workspace_bytes(), device)
+
+        def rope_once():
+            h3r.qk_norm_rope(qkv_out, wq, wk, pos, c["heads"], c["rot"], c["axis_dims"], c["theta"], c["eps"],
+                             workspace=ws_r)
+
+        for _ in range(max(3, a.warmup)):
+            rope_once()
+        n_r = max(10, a.steps // 4)
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        r0.record()
+        for _ in range(n_r):
+            rope_once()
+        r1.record()
+        torch.cuda.synchronize()
+        if h3r.read_status(ws_r) != 0:
+            raise RuntimeError("device status set by h3lin_qk_norm_rope")
+        rms = r0.elapsed_time(r1) / n_r
+        rbytes = S * 2 * c["heads"] * 128 * 2 * 2 + S * 12
+        rope_line = {"ms": rms, "launches": n_r, "algorithmic_bytes": rbytes,
+                     "achieved_gbs": rbytes / (rms * 1e-3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
+                     "frac": rbytes / (rms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm",
+                     "what": "h3lin_qk_norm_rope in place on the block's QKV output [S, 15360] bf16: per-head "
+                             "RMSNorm of Q and K, split-half RoPE of 96 of 128 dims over (t, h, w) positions; "
+                             "bytes = Q and K read and written once + positions"}
+
     # merged-LoRA comparison mode: each weight with its adapter folded in
     # (h3lin_merge_lora), re-packed, then the block on the base path only
     merged_line = None
@@ -593,6 +633,7 @@ def native_arm(a, rank, world, local_rank):
             "flops_per_block": {"total": total, "base_fp4": base, "lora_down": ldown, "lora_up": lup},
             "kernel_ms": {"gemm": gemm_total_ms, "prepare": ms - gemm_total_ms},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "merged_lora": merged_line,
+            "qk_norm_rope": rope_line,
             "gpu_launches": blk.launches_per_step() * a.steps, "clocks": clocks,
             "peaks": {"kind": peak_kind, **peaks}}
     print(json.dumps(line), flush=True)

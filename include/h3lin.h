@@ -266,6 +266,50 @@ h3lin_status h3lin_mlp_forward(const void* x, int64_t M,
 h3lin_status h3lin_merge_lora(const void* w, int64_t N, int64_t K, const float* pre_quant_scale,
                               const h3lin_adapter* adapter, float strength, void* w_out, cudaStream_t stream);
 
+/* ------------------------------------- Q/K RMSNorm + split-half RoPE step */
+/* The step after the fused QKV projection (MiniMax-H3 Ultra Fast README,
+ * "Active optimization stack", row "Attention projections": one fused in-place
+ * Q/K RMSNorm + partial split-half RoPE kernel per block; "Kernel path", item
+ * 2: three-axis split-half rotary embedding; head size 128 with 96 rotated
+ * dimensions: MiniMax-H3 Turbo — one file, no Python, the list of conventions
+ * before "Two clocks").  In place on the projection's bf16 output
+ * qkv [M, 3 * heads * head_dim] = [Q | K | V] (head-major), for every row m
+ * and every head of Q (gain q_gain) and of K (gain k_gain):
+ *
+ *   y[d]   = x[d] / sqrt(mean_d(x^2) + eps) * gain[d]            (fp32)
+ *   pair i < rot/2 of axis a (t, h, w: pairs concatenated in that order,
+ *   axis_dims[a] / 2 each; j = i minus the pairs of the earlier axes):
+ *     angle  = float(positions[m, a]) * theta^(-2 j / axis_dims[a])
+ *     out[i]         = y[i] cos(angle) - y[i + rot/2] sin(angle)
+ *     out[i + rot/2] = y[i + rot/2] cos(angle) + y[i] sin(angle)
+ *   out[d] = y[d] for rot <= d < head_dim;  stored as bf16 (round to nearest)
+ *
+ * V is not touched.  The frequencies are computed on the host in double and
+ * rounded to float; angles in float, then sincosf.
+ *   qkv        device bf16, 16-byte aligned; rows >= M never touched
+ *   q_gain, k_gain  device fp32 [head_dim], 16-byte aligned
+ *   positions  device int32 [M, 3] (t, h, w), 4-byte aligned
+ *   workspace  >= h3lin_quant_workspace_bytes(), initialised once; only its
+ *              status word is used (a timed-out device wait records
+ *              H3LIN_E_TIMEOUT there, read with h3lin_read_status)
+ * Rules: head_dim == 128; rot_dims % 16 == 0, 16 <= rot_dims <= head_dim;
+ * axis_dims even, >= 0, summing to rot_dims; heads >= 1; theta > 0 and eps
+ * >= 0 finite; M >= 0 (M == 0: no-op).  Errors: H3LIN_E_INVALID (null
+ * pointer or parameter), H3LIN_E_SHAPE, H3LIN_E_ALIGN, H3LIN_E_UNSUPPORTED,
+ * H3LIN_E_CUDA; nothing is enqueued on error.  Allocates nothing. */
+typedef struct {
+  int32_t heads;        /* heads of Q and of K */
+  int32_t head_dim;     /* 128 */
+  int32_t rot_dims;     /* rotated dimensions per head (96) */
+  int32_t axis_dims[3]; /* rotated dimensions per position axis t, h, w */
+  float theta;          /* frequency base (10000) */
+  float eps;            /* RMSNorm epsilon (1e-6) */
+} h3lin_rope_params;
+
+h3lin_status h3lin_qk_norm_rope(void* qkv, int64_t M, const h3lin_rope_params* params, const float* q_gain,
+                                const float* k_gain, const int32_t* positions, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------- failure self-test */
 /* Exercises the kernels' failure path on the device without any fault: a
  * kernel waits, with a bound of `wait_cycles` SM clock cycles (1 .. 2^31), on

@@ -511,6 +511,38 @@ h3lin_status h3lin_read_status(const void* ws, cudaStream_t stream, int32_t* dev
 
 }  // extern "C"
 
+extern "C" h3lin_status h3lin_qk_norm_rope(void* qkv, int64_t M, const h3lin_rope_params* p, const float* q_gain,
+                                           const float* k_gain, const int32_t* positions, void* ws,
+                                           size_t ws_bytes, cudaStream_t stream) {
+  if (!p) return H3LIN_E_INVALID;
+  if (!std::isfinite(p->theta) || !(p->theta > 0.0f) || !std::isfinite(p->eps) || p->eps < 0.0f)
+    return H3LIN_E_INVALID;
+  if (M < 0 || M > kMaxDim || p->heads < 1 || p->head_dim != 128 || p->rot_dims < 16 ||
+      p->rot_dims > p->head_dim || p->rot_dims % 16 != 0 || int64_t(p->heads) * 3 * p->head_dim > kMaxDim)
+    return H3LIN_E_SHAPE;
+  int64_t sum = 0;
+  for (int a = 0; a < 3; ++a) {
+    if (p->axis_dims[a] < 0 || p->axis_dims[a] % 2 != 0) return H3LIN_E_SHAPE;
+    sum += p->axis_dims[a];
+  }
+  if (sum != p->rot_dims) return H3LIN_E_SHAPE;
+  if (M == 0) return H3LIN_OK;
+  if (!qkv || !q_gain || !k_gain || !positions || !ws) return H3LIN_E_INVALID;
+  if (!aligned16(qkv) || !aligned16(q_gain) || !aligned16(k_gain) || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u))
+    return H3LIN_E_ALIGN;
+  if (ws_bytes < kHeaderBytes) return H3LIN_E_WORKSPACE;
+  DeviceInfo d;
+  const h3lin_status s = require_device(&d);
+  if (s != H3LIN_OK) return s;
+  const int axis[3] = {p->axis_dims[0], p->axis_dims[1], p->axis_dims[2]};
+  if (launch_qk_norm_rope(qkv, int(M), p->heads, p->rot_dims, axis, p->theta, p->eps, q_gain, k_gain, positions,
+                          reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + kStatusOffset), d.sm_count,
+                          stream) != cudaSuccess)
+    return H3LIN_E_CUDA;
+  return H3LIN_OK;
+}
+
 extern "C" h3lin_status h3lin_merge_lora(const void* w, int64_t N, int64_t K, const float* pre_quant_scale,
                                          const h3lin_adapter* adapter, float strength, void* w_out,
                                          cudaStream_t stream) {

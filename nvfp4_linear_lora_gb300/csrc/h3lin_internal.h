@@ -81,6 +81,12 @@ cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st);
 // tile_rows rows (h3lin_gemm.cu).
 int raster_group(int64_t N, int64_t K, int tile_rows);
 
+// Q/K RMSNorm + split-half three-axis RoPE in place on qkv [M, 3 heads 128]
+// (h3lin_rope.cu; arguments validated by h3lin_qk_norm_rope).
+cudaError_t launch_qk_norm_rope(void* qkv, int M, int heads, int rot, const int (&axis_dims)[3], float theta,
+                                float eps, const float* q_gain, const float* k_gain, const int* pos,
+                                uint32_t* status, int sm_count, cudaStream_t st);
+
 // W'[N, K] = bf16(W + c * (B[N, r] @ A[r, K]) / s[K]) (h3lin_merge.cu; s may be
 // null = 1); in place allowed.
 cudaError_t launch_merge_lora(const void* w, const void* A, const void* B, const float* pqs, void* w_out, int N,

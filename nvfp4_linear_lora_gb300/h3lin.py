@@ -46,6 +46,11 @@ class h3lin_adapter(ctypes.Structure):
                 ("alpha", ctypes.c_float)]
 
 
+class h3lin_rope_params(ctypes.Structure):
+    _fields_ = [("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("rot_dims", ctypes.c_int32),
+                ("axis_dims", ctypes.c_int32 * 3), ("theta", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
 _lib = None
 _vp, _i64, _i32, _sz, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
 
@@ -73,6 +78,7 @@ _SIGNATURES = {
     "h3lin_mlp_forward": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter), _f32,
                                  _vp, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter), _f32,
                                  _vp, _vp, _i32, _vp, _sz, _vp]),
+    "h3lin_qk_norm_rope": (_i32, [_vp, _i64, ctypes.POINTER(h3lin_rope_params), _vp, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "h3lin_selftest_wait_timeout": (_i32, [_vp, _sz, _i64, _vp]),
     "h3lin_merge_lora": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(h3lin_adapter), _f32, _vp, _vp]),
@@ -177,6 +183,10 @@ def h3lin_mlp_forward(x, M, gu_pqs, gate_up, gu_adapter, gu_strength, down_pqs, 
     return lib().h3lin_mlp_forward(x, M, gu_pqs, _ref(gate_up), _ref(gu_adapter), gu_strength, down_pqs,
                                    _ref(down), _ref(down_adapter), down_strength, h, out, out_dtype, ws, ws_bytes,
                                    stream)
+
+
+def h3lin_qk_norm_rope(qkv, M, params, q_gain, k_gain, positions, ws, ws_bytes, stream):
+    return lib().h3lin_qk_norm_rope(qkv, M, _ref(params), q_gain, k_gain, positions, ws, ws_bytes, stream)
 
 
 def h3lin_forward_noalloc(x, M, pqs, weight, epilogue, adapter, strength, out, out_dtype, stream):
@@ -329,6 +339,27 @@ def mlp_forward(x, gate_up, down, gate_up_pre_quant_scale=None, down_pre_quant_s
                              h.data_ptr(), out.data_ptr(), code, workspace.data_ptr(), workspace.numel(),
                              _stream()), "h3lin_mlp_forward")
     return h, out
+
+
+def rope_params(heads, head_dim=128, rot_dims=96, axis_dims=(32, 32, 32), theta=10000.0, eps=1e-6):
+    return h3lin_rope_params(heads, head_dim, rot_dims, (ctypes.c_int32 * 3)(*axis_dims), theta, eps)
+
+
+def qk_norm_rope(qkv, q_gain, k_gain, positions, heads, rot_dims=96, axis_dims=(32, 32, 32), theta=10000.0,
+                 eps=1e-6, workspace=None):
+    """In place on ``qkv`` bf16 [M, 3 * heads * 128]: per-head RMSNorm of Q and K
+    (gains fp32 [128]) and split-half three-axis RoPE from ``positions`` int32
+    [M, 3]; returns ``qkv``."""
+    torch = _torch()
+    if qkv.dtype != torch.bfloat16 or qkv.dim() != 2 or not qkv.is_contiguous():
+        raise TypeError("qkv must be a contiguous 2-D bfloat16 tensor")
+    if positions.dtype != torch.int32:
+        raise TypeError("positions must be int32 [M, 3]")
+    p = rope_params(heads, 128, rot_dims, axis_dims, theta, eps)
+    ws = workspace if workspace is not None else new_workspace(h3lin_quant_workspace_bytes(), qkv.device)
+    _check(h3lin_qk_norm_rope(qkv.data_ptr(), qkv.shape[0], p, q_gain.data_ptr(), k_gain.data_ptr(),
+                              positions.data_ptr(), ws.data_ptr(), ws.numel(), _stream()), "h3lin_qk_norm_rope")
+    return qkv
 
 
 def merge_lora(w, adapter, strength=1.0, pre_quant_scale=None, out=None):

@@ -183,6 +183,35 @@ def test_mlp_and_producer_argument_checks():
     assert h3lin.h3lin_forward_prepare_produced(None, 5, None, dn, None, 1.0, A, 1 << 30, None) == E.H3LIN_E_INVALID
 
 
+def test_qk_norm_rope_argument_checks():
+    E = h3lin
+
+    def call(M=10, qkv=A, qg=A, kg=A, pos=A, ws=A, ws_bytes=1 << 20, **kw):
+        prm = dict(heads=40, head_dim=128, rot_dims=96, axis_dims=(32, 32, 32), theta=10000.0, eps=1e-6)
+        prm.update(kw)
+        return h3lin.h3lin_qk_norm_rope(qkv, M, h3lin.rope_params(**prm), qg, kg, pos, ws, ws_bytes, None)
+
+    assert h3lin.h3lin_qk_norm_rope(A, 10, None, A, A, A, A, 1 << 20, None) == E.H3LIN_E_INVALID
+    assert call(head_dim=64) == E.H3LIN_E_SHAPE
+    assert call(rot_dims=100, axis_dims=(34, 34, 32)) == E.H3LIN_E_SHAPE     # rot % 16
+    assert call(rot_dims=144, axis_dims=(48, 48, 48)) == E.H3LIN_E_SHAPE     # rot > head_dim
+    assert call(axis_dims=(32, 32, 30)) == E.H3LIN_E_SHAPE                   # sum != rot
+    assert call(axis_dims=(31, 33, 32)) == E.H3LIN_E_SHAPE                   # odd axis
+    assert call(heads=0) == E.H3LIN_E_SHAPE
+    assert call(M=-1) == E.H3LIN_E_SHAPE
+    assert call(theta=0.0) == E.H3LIN_E_INVALID
+    assert call(eps=-1.0) == E.H3LIN_E_INVALID
+    assert call(eps=math.nan) == E.H3LIN_E_INVALID
+    assert call(M=0, qkv=None, qg=None, kg=None, pos=None, ws=None) == E.H3LIN_OK
+    assert call(qkv=None) == E.H3LIN_E_INVALID
+    assert call(qkv=A + 8) == E.H3LIN_E_ALIGN
+    assert call(qg=A + 4) == E.H3LIN_E_ALIGN
+    assert call(pos=A + 2) == E.H3LIN_E_ALIGN
+    assert call(ws=None) == E.H3LIN_E_INVALID
+    assert call(ws=A + 8) == E.H3LIN_E_ALIGN
+    assert call(ws_bytes=64) == E.H3LIN_E_WORKSPACE
+
+
 def test_mlp_workspace_is_the_larger_projection_workspace():
     M, K, Ngu, Nd, r = 37726, 5120, 27648, 5120, 128
     want = max(h3lin.h3lin_forward_workspace_bytes(M, K, Ngu, r), h3lin.h3lin_forward_workspace_bytes(M, Ngu // 2, Nd, r))
