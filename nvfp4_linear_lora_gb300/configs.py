@@ -40,6 +40,12 @@ SWEEP_M = (1024, 4096, 16384, 37726, 65536)
 ROPE = dict(heads=HIDDEN // 128, head_dim=128, rot=96, axis_dims=(32, 32, 32), theta=10000.0, eps=1e-6,
             frames=9, height=48, width=84)
 ROPE_SEED = 8
+
+# Modulation producer: the packed sequence's rows in three segments, each
+# gathering its own AdaLN table row (video 9 x 48 x 84 latent patches, then
+# the audio and text rows); LayerNorm epsilon 1e-6.
+MODULATION = dict(segments=(9 * 48 * 84, 1022, 416), eps=1e-6)
+MODULATION_SEED = 9
 SWEEP_SEEDS = (3, 4, 5, 6, 7)
 
 

@@ -14,7 +14,10 @@ Value laws (one per workload, see ``configs.py``):
 * base weight ``W``: N(0, 1/K), rounded to bf16 before NVFP4 packing;
 * LoRA ``A [r, K]``: N(0, 1/K); ``B [N, r]``: 0.1 * N(0, 1/r); both bf16;
 * Q/K RMSNorm gains: 1 + 0.1 * N(0, 1); RoPE positions: integer video-grid
-  coordinates (``rope_positions``), no randomness.
+  coordinates (``rope_positions``), no randomness;
+* residual stream (modulation input): per-row N(0, 1) * U(0.5, 4) + N(0, 1),
+  bf16; AdaLN table: 0.1 * N(0, 1) shift and scale per table row; segment
+  table: consecutive runs of rows per table row.
 
 Draw order inside one generator: x, outlier channel indices, s, W, A, B.
 """
@@ -82,6 +85,25 @@ def adapter(rng, N, K, rank, alpha=None):
     A = bf16_round(_normal(rng, (rank, K), std=1.0 / np.sqrt(K)))
     B = bf16_round(_normal(rng, (N, rank), std=0.1 / np.sqrt(rank)))
     return {"A": A, "B": B, "rank": int(rank), "alpha": float(rank if alpha is None else alpha)}
+
+
+def residual(rng, M, K):
+    """A residual-stream stand-in, bf16 [M, K]: per row a N(0, 1) draw scaled by
+    U(0.5, 4) and shifted by N(0, 1) (rows with different means and spreads)."""
+    g = rng.uniform(0.5, 4.0, (M, 1)).astype(np.float32)
+    o = rng.standard_normal((M, 1)).astype(np.float32)
+    return bf16_round(_normal(rng, (M, K)) * g + o)
+
+
+def adaln_table(rng, T, K):
+    """AdaLN modulation table, float32 [T, 2, K]: (shift, scale) per distinct
+    timestep, both 0.1 * N(0, 1)."""
+    return (0.1 * rng.standard_normal((T, 2, K))).astype(np.float32)
+
+
+def segment_rows(sizes):
+    """Table row of every packed row, int32: ``sizes[t]`` consecutive rows use row t."""
+    return np.concatenate([np.full(n, t, np.int32) for t, n in enumerate(sizes)])
 
 
 def norm_gain(rng, D):
