@@ -79,6 +79,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-merged", action="store_true",
                     help="skip the merged-LoRA comparison (weights with the adapter folded in, base path only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU-oracle sample time")
+    ap.add_argument("--no-modulation", action="store_true",
+                    help="skip the modulation-producer measurement on the block's QKV input")
     ap.add_argument("--no-rope", action="store_true",
                     help="skip the Q/K RMSNorm + RoPE measurement on the block's QKV output")
     ap.add_argument("--unfused-mlp", action="store_true",
@@ -473,6 +475,59 @@ def native_arm(a, rank, world, local_rank):
                              "RMSNorm of Q and K, split-half RoPE of 96 of 128 dims over (t, h, w) positions; "
                              "bytes = Q and K read and written once + positions"}
 
+    # the step before QKV: the modulation producer (LayerNorm + segment-wise
+    # AdaLN shift/scale -> bf16 LoRA input + amax partials), then QKV's prepare
+    # from those partials (one pass over x_mod) against the plain prepare
+    mod_line = None
+    if not a.no_modulation:
+        c = configs.MODULATION
+        h3m = blk.h3lin
+        mrng = np.random.default_rng(configs.MODULATION_SEED)
+        xres = synth.to_bf16_tensor(synth.residual(mrng, S, configs.HIDDEN)).to(device)
+        tab = torch.from_numpy(synth.adaln_table(mrng, len(c["segments"]), configs.HIDDEN)).to(device)
+        rtab = torch.from_numpy(synth.segment_rows(c["segments"])).to(device)
+        q = blk.proj[0]
+        xmod = torch.empty_like(xres)
+
+        def mod_once():
+            h3m.modulate_produce(xres, tab, rtab, q["ws"], q["pqs_dev"], c["eps"], out=xmod)
+
+        def timed(fn, n):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / n
+
+        n_m = max(10, a.steps // 4)
+        mms_ = timed(mod_once, n_m)
+
+        def prep(fn):
+            st = fn(xmod.data_ptr(), S, q["pqs_dev"].data_ptr(), q["wc"], q["ac"], 1.0, q["ws"].data_ptr(),
+                    q["ws"].numel(), q["stream"])
+            if st:
+                raise h3m.H3linError(st, "prepare")
+
+        mod_once()
+        p_prod = timed(lambda: prep(h3m.h3lin_forward_prepare_produced), n_m)
+        p_plain = timed(lambda: prep(h3m.h3lin_forward_prepare), n_m)
+        if h3m.read_status(q["ws"]) != 0:
+            raise RuntimeError("device status set by the modulation producer")
+        mbytes = S * configs.HIDDEN * 4 + S * 4
+        mod_line = {"ms": mms_, "launches": n_m, "algorithmic_bytes": mbytes,
+                    "achieved_gbs": mbytes / (mms_ * 1e-3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
+                    "frac": mbytes / (mms_ * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm",
+                    "qkv_prepare_from_partials_ms": p_prod, "qkv_prepare_plain_ms": p_plain,
+                    "what": "h3lin_modulate_produce on the block's QKV input [S, 5120]: LayerNorm + (1 + scale) "
+                            "and shift gathered from a 3-row AdaLN table by segment, bf16 out, amax partials for "
+                            "QKV; bytes = x read + x_mod written once. Then QKV's prepare from those partials "
+                            "(one pass over x_mod: quantise + A(x)) vs the plain prepare (amax pass + quantise)"}
+
     # merged-LoRA comparison mode: each weight with its adapter folded in
     # (h3lin_merge_lora), re-packed, then the block on the base path only
     merged_line = None
@@ -633,7 +688,7 @@ def native_arm(a, rank, world, local_rank):
             "flops_per_block": {"total": total, "base_fp4": base, "lora_down": ldown, "lora_up": lup},
             "kernel_ms": {"gemm": gemm_total_ms, "prepare": ms - gemm_total_ms},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "merged_lora": merged_line,
-            "qk_norm_rope": rope_line,
+            "qk_norm_rope": rope_line, "modulation": mod_line,
             "gpu_launches": blk.launches_per_step() * a.steps, "clocks": clocks,
             "peaks": {"kind": peak_kind, **peaks}}
     print(json.dumps(line), flush=True)

@@ -266,6 +266,38 @@ h3lin_status h3lin_mlp_forward(const void* x, int64_t M,
 h3lin_status h3lin_merge_lora(const void* w, int64_t N, int64_t K, const float* pre_quant_scale,
                               const h3lin_adapter* adapter, float strength, void* w_out, cudaStream_t stream);
 
+/* ------------------------------------------------ modulation producer */
+/* The input of the QKV and gate/up projections: the residual stream
+ * normalised and modulated by the AdaLN table, one table row per distinct
+ * timestep gathered segment-wise over the packed sequence (MiniMax-H3 Ultra
+ * Fast README, "Active optimization stack", row "AdaLN"), emitted as the
+ * exact BF16 LoRA input while the NVFP4 packing's amax is reduced on the way
+ * (TURBO.md, h3-blackwell-runtime, "Implementation": modulation producer):
+ *
+ *   y     = (x - mean) / sqrt(var + eps)   per row over K, population variance, fp32
+ *   x_mod = bf16(y * (1 + scale[t]) + shift[t]),  t = row_table[row]
+ *
+ * and, in the consuming projection's workspace, the amax partials of
+ * |x_mod * next_pre_quant_scale| that h3lin_forward_prepare_produced reads
+ * (one pass over x_mod instead of two; the result is bit-identical to
+ * h3lin_forward on x_mod).
+ *   x          device bf16 [M, K], 16-byte aligned
+ *   table      device fp32 [table_rows, 2, K]: (shift, scale) per row, 16-byte aligned
+ *   row_table  device int32 [M]: table row of every row; an entry outside
+ *              [0, table_rows) records H3LIN_E_INVALID in next_workspace's
+ *              status word and that row is written as zeros
+ *   x_mod      device bf16 [M, K] (output), 16-byte aligned
+ *   next_pre_quant_scale  the consumer's pre_quant_scale, fp32 [K] or NULL
+ *   next_workspace        the consumer's workspace (>= header size, 16-byte aligned)
+ * Rules: K % 64 == 0, 64 <= K <= 8192; table_rows >= 1; eps >= 0 finite;
+ * M >= 0 (0: no-op).  Errors: H3LIN_E_SHAPE, H3LIN_E_INVALID, H3LIN_E_ALIGN,
+ * H3LIN_E_WORKSPACE, H3LIN_E_UNSUPPORTED, H3LIN_E_CUDA; nothing is enqueued
+ * on error.  Allocates nothing. */
+h3lin_status h3lin_modulate_produce(const void* x, int64_t M, int64_t K, const float* table, int32_t table_rows,
+                                    const int32_t* row_table, float eps, void* x_mod,
+                                    const float* next_pre_quant_scale, void* next_workspace,
+                                    size_t next_workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------- Q/K RMSNorm + split-half RoPE step */
 /* The step after the fused QKV projection (MiniMax-H3 Ultra Fast README,
  * "Active optimization stack", row "Attention projections": one fused in-place

@@ -543,6 +543,29 @@ extern "C" h3lin_status h3lin_qk_norm_rope(void* qkv, int64_t M, const h3lin_rop
   return H3LIN_OK;
 }
 
+extern "C" h3lin_status h3lin_modulate_produce(const void* x, int64_t M, int64_t K, const float* table,
+                                               int32_t table_rows, const int32_t* row_table, float eps, void* x_mod,
+                                               const float* next_pqs, void* next_ws, size_t next_ws_bytes,
+                                               cudaStream_t stream) {
+  if (M < 0 || M > kMaxDim || K < 64 || K > 8192 || K % 64 != 0 || table_rows < 1) return H3LIN_E_SHAPE;
+  if (!std::isfinite(eps) || eps < 0.0f) return H3LIN_E_INVALID;
+  if (M == 0) return H3LIN_OK;
+  if (!x || !table || !row_table || !x_mod || !next_ws) return H3LIN_E_INVALID;
+  if (!aligned16(x) || !aligned16(table) || !aligned16(x_mod) || !aligned16(next_ws) ||
+      (next_pqs && !aligned16(next_pqs)) || (reinterpret_cast<uintptr_t>(row_table) & 3u))
+    return H3LIN_E_ALIGN;
+  if (next_ws_bytes < kHeaderBytes) return H3LIN_E_WORKSPACE;
+  DeviceInfo d;
+  const h3lin_status s = require_device(&d);
+  if (s != H3LIN_OK) return s;
+  uint8_t* w = static_cast<uint8_t*>(next_ws);
+  if (launch_modulate(x, int(M), int(K), table, table_rows, row_table, eps, x_mod, next_pqs,
+                      reinterpret_cast<float*>(w + kPartialsOffset), reinterpret_cast<int*>(w + kProducedOffset),
+                      reinterpret_cast<uint32_t*>(w + kStatusOffset), d.sm_count, stream) != cudaSuccess)
+    return H3LIN_E_CUDA;
+  return H3LIN_OK;
+}
+
 extern "C" h3lin_status h3lin_merge_lora(const void* w, int64_t N, int64_t K, const float* pre_quant_scale,
                                          const h3lin_adapter* adapter, float strength, void* w_out,
                                          cudaStream_t stream) {

@@ -87,6 +87,12 @@ cudaError_t launch_qk_norm_rope(void* qkv, int M, int heads, int rot, const int 
                                 float eps, const float* q_gain, const float* k_gain, const int* pos,
                                 uint32_t* status, int sm_count, cudaStream_t st);
 
+// Modulation producer (h3lin_modulate.cu): x_mod = bf16(LN(x) (1 + scale) +
+// shift) per row's table row, plus amax partials of |x_mod * pqs| and their count.
+cudaError_t launch_modulate(const void* x, int M, int K, const float* table, int T, const int* row_table, float eps,
+                            void* out, const float* pqs, float* partials, int* count, uint32_t* status, int sm_count,
+                            cudaStream_t st);
+
 // W'[N, K] = bf16(W + c * (B[N, r] @ A[r, K]) / s[K]) (h3lin_merge.cu; s may be
 // null = 1); in place allowed.
 cudaError_t launch_merge_lora(const void* w, const void* A, const void* B, const float* pqs, void* w_out, int N,

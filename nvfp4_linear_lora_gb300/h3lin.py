@@ -79,6 +79,7 @@ _SIGNATURES = {
                                  _vp, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter), _f32,
                                  _vp, _vp, _i32, _vp, _sz, _vp]),
     "h3lin_qk_norm_rope": (_i32, [_vp, _i64, ctypes.POINTER(h3lin_rope_params), _vp, _vp, _vp, _vp, _sz, _vp]),
+    "h3lin_modulate_produce": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "h3lin_selftest_wait_timeout": (_i32, [_vp, _sz, _i64, _vp]),
     "h3lin_merge_lora": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(h3lin_adapter), _f32, _vp, _vp]),
@@ -187,6 +188,12 @@ def h3lin_mlp_forward(x, M, gu_pqs, gate_up, gu_adapter, gu_strength, down_pqs, 
 
 def h3lin_qk_norm_rope(qkv, M, params, q_gain, k_gain, positions, ws, ws_bytes, stream):
     return lib().h3lin_qk_norm_rope(qkv, M, _ref(params), q_gain, k_gain, positions, ws, ws_bytes, stream)
+
+
+def h3lin_modulate_produce(x, M, K, table, table_rows, row_table, eps, x_mod, next_pqs, next_ws, next_ws_bytes,
+                           stream):
+    return lib().h3lin_modulate_produce(x, M, K, table, table_rows, row_table, eps, x_mod, next_pqs, next_ws,
+                                        next_ws_bytes, stream)
 
 
 def h3lin_forward_noalloc(x, M, pqs, weight, epilogue, adapter, strength, out, out_dtype, stream):
@@ -360,6 +367,42 @@ def qk_norm_rope(qkv, q_gain, k_gain, positions, heads, rot_dims=96, axis_dims=(
     _check(h3lin_qk_norm_rope(qkv.data_ptr(), qkv.shape[0], p, q_gain.data_ptr(), k_gain.data_ptr(),
                               positions.data_ptr(), ws.data_ptr(), ws.numel(), _stream()), "h3lin_qk_norm_rope")
     return qkv
+
+
+def modulate_produce(x, table, row_table, next_workspace, next_pre_quant_scale=None, eps=1e-6, out=None):
+    """x_mod = bf16(LayerNorm(x) * (1 + scale) + shift) with the table row of each
+    row (``table`` fp32 [T, 2, K], ``row_table`` int32 [M]); leaves the amax of
+    |x_mod * next_pre_quant_scale| in ``next_workspace`` for
+    ``h3lin_forward_prepare_produced``.  Returns x_mod (bf16 [M, K])."""
+    torch = _torch()
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    _check(h3lin_modulate_produce(x.data_ptr(), M, K, table.data_ptr(), table.shape[0], row_table.data_ptr(),
+                                  float(eps), out.data_ptr(), _ptr(next_pre_quant_scale), next_workspace.data_ptr(),
+                                  next_workspace.numel(), _stream()), "h3lin_modulate_produce")
+    return out
+
+
+def forward_produced(x, weight, workspace, pre_quant_scale=None, adapter=None, strength=1.0, silu_mul=False,
+                     out=None, out_dtype=None):
+    """A projection whose input x was written by a producer (modulation or a
+    producer GEMM) that left its amax in ``workspace``: prepare from those
+    partials (one pass over x), then the GEMM.  Same result as ``forward``."""
+    torch = _torch()
+    M = x.shape[0]
+    n_out = weight.N // 2 if silu_mul else weight.N
+    if out is None:
+        out = torch.empty((M, n_out), dtype=out_dtype or torch.bfloat16, device=x.device)
+    code = H3LIN_OUT_F32 if out.dtype == torch.float32 else H3LIN_OUT_BF16
+    wc = weight.c_struct()
+    ac = adapter.c_struct() if adapter is not None else None
+    st = _stream()
+    _check(h3lin_forward_prepare_produced(x.data_ptr(), M, _ptr(pre_quant_scale), wc, ac, float(strength),
+                                          workspace.data_ptr(), workspace.numel(), st), "h3lin_forward_prepare_produced")
+    _check(h3lin_forward_gemm(M, wc, H3LIN_EPI_SILU_MUL if silu_mul else H3LIN_EPI_NONE, ac, float(strength),
+                              out.data_ptr(), code, workspace.data_ptr(), workspace.numel(), st), "h3lin_forward_gemm")
+    return out
 
 
 def merge_lora(w, adapter, strength=1.0, pre_quant_scale=None, out=None):

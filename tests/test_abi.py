@@ -212,6 +212,26 @@ def test_qk_norm_rope_argument_checks():
     assert call(ws_bytes=64) == E.H3LIN_E_WORKSPACE
 
 
+def test_modulate_produce_argument_checks():
+    E = h3lin
+
+    def call(x=A, M=10, K=5120, table=A, T=3, rows=A, eps=1e-6, out=A, pqs=None, ws=A, ws_bytes=1 << 20):
+        return h3lin.h3lin_modulate_produce(x, M, K, table, T, rows, eps, out, pqs, ws, ws_bytes, None)
+
+    assert call(K=96) == E.H3LIN_E_SHAPE
+    assert call(K=8256) == E.H3LIN_E_SHAPE
+    assert call(T=0) == E.H3LIN_E_SHAPE
+    assert call(M=-2) == E.H3LIN_E_SHAPE
+    assert call(eps=math.inf) == E.H3LIN_E_INVALID
+    assert call(M=0, x=None, table=None, rows=None, out=None, ws=None) == E.H3LIN_OK
+    assert call(table=None) == E.H3LIN_E_INVALID
+    assert call(ws=None) == E.H3LIN_E_INVALID
+    assert call(out=A + 4) == E.H3LIN_E_ALIGN
+    assert call(rows=A + 2) == E.H3LIN_E_ALIGN
+    assert call(pqs=A + 8) == E.H3LIN_E_ALIGN
+    assert call(ws_bytes=100) == E.H3LIN_E_WORKSPACE
+
+
 def test_mlp_workspace_is_the_larger_projection_workspace():
     M, K, Ngu, Nd, r = 37726, 5120, 27648, 5120, 128
     want = max(h3lin.h3lin_forward_workspace_bytes(M, K, Ngu, r), h3lin.h3lin_forward_workspace_bytes(M, Ngu // 2, Nd, r))
