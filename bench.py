@@ -89,6 +89,23 @@ def parse_args(argv=None):
     return ap.parse_args(argv)
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time: every rank contributes its own, all get the max
+    (replicas: the job is done when the last one is)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank, world, ms):
+    """Whole-job throughput: every rank processes its own block (weak scaling)."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -431,11 +448,8 @@ def native_arm(a, rank, world, local_rank):
     gemm_ms = [statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(a.steps))
                for i in range(len(blk.proj))]
     blk.check_status()
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * total / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(ms, world, device)
+    value = whole_job_tflops(total, world, ms)
 
     # the step after QKV: Q/K RMSNorm + split-half three-axis RoPE, in place on
     # the block's QKV output (1.16 GB, larger than L2), timed alone
@@ -567,10 +581,7 @@ def native_arm(a, rank, world, local_rank):
         finally:
             for d, (wc, ac) in zip(blk.proj, saved):
                 d["wc"], d["ac"] = wc, ac
-        if world > 1:
-            t = torch.tensor([mms], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            mms = float(t.item())
+        mms = max_over_ranks(mms, world, device)
         merged_line = {"ms_per_block": mms, "steps": n_m,
                        "base_tflops": world * base / (mms * 1e-3) / 1e12,
                        "dynamic_over_merged_time": ms / mms,
@@ -632,10 +643,7 @@ def native_arm(a, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
         ems = e0.elapsed_time(e1) / a.e2e_steps
-        if world > 1:
-            t = torch.tensor([ems], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(ems, world, device)
         blk.check_status()
         e2e = {"value": world * total / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
