@@ -135,7 +135,14 @@ struct QuantCtx {
   int kb, K;
   uint2* codes;      // 8 bytes = 16 codes per block
   uint8_t* scales;
+  const float* inv_tab;   // optional: 1 / (E4M3(sb) * ts) for every scale byte sb (shared memory)
 };
+
+// inv_tab[sb] = 1 / fl(E4M3(sb) * ts), the same two roundings quant_block takes
+// per block, tabulated once per CTA for the 256 scale bytes.
+__device__ __forceinline__ float block_inv(float ts, uint32_t sb) {
+  return __frcp_rn(__fmul_rn(e4m3_to_float(sb), ts));
+}
 
 __device__ __forceinline__ void load_scale16(const float* __restrict__ pqs, int b, float (&s)[16]) {
   if (pqs == nullptr) {
@@ -169,8 +176,7 @@ __device__ __forceinline__ void quant_block(const QuantCtx& q, int row, int b, c
 #pragma unroll
   for (int i = 1; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
   const uint32_t sb = e4m3_rn_satfinite(__fdiv_rn(bm, q.six_ts));
-  const float d = __fmul_rn(e4m3_to_float(sb), q.ts);
-  const float inv = __frcp_rn(d);
+  const float inv = q.inv_tab ? q.inv_tab[sb] : block_inv(q.ts, sb);
   float qa[8], qb[8];
 #pragma unroll
   for (int i = 0; i < 8; i += 2) {
@@ -203,7 +209,7 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant(
   if (ts == 0.0f) ts = 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
   const int kb = K >> 4;
-  QuantCtx q{ts, __fmul_rn(6.0f, ts), kb, K, codes, scales};
+  QuantCtx q{ts, __fmul_rn(6.0f, ts), kb, K, codes, scales, nullptr};
 
   const int tid = blockIdx.x * kQuantThreads + threadIdx.x;
   const int b = tid % kb;
@@ -269,9 +275,12 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant(
 constexpr int kLoraAmaxWarps = 8;
 constexpr int kLoraRowStride = 32 * kLoraAmaxWarps / 8;   // rows between a thread's rows
 static_assert(128 % kLoraRowStride == 0, "rows of a tile per amax thread");
-// The quantising variant does several times the ALU work per byte of the amax
-// pass, so it runs twice the worker warps.
-constexpr int kLoraQuantWarps = 16;
+// Worker warps per CTA of the quantising variant.  Two CTAs share an SM when
+// the TMEM accumulator and the ring fit twice (rank <= 256): each CTA's
+// pipeline (ring fill, tile epilogue, stalls) then overlaps the other's, which
+// measured faster than one CTA with twice the workers.
+constexpr int kLoraQuantWarps = 8;
+constexpr bool kLoraAmaxTwoCtas = true;   // the amax pass takes two CTAs per SM as well
 template <bool QUANT> constexpr int lora_workers() { return QUANT ? kLoraQuantWarps : kLoraAmaxWarps; }
 template <bool QUANT> constexpr int lora_threads() { return 64 + 32 * lora_workers<QUANT>(); }
 
@@ -293,7 +302,7 @@ struct QuantPassOut {
 };
 
 template <bool QUANT>
-__global__ void __launch_bounds__(lora_threads<QUANT>(), 1) k_amax_lora(
+__global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a, int M, int K,
     int rank, int a_box_rows, const float* __restrict__ pqs, float* __restrict__ partials,
     __nv_bfloat16* __restrict__ u, uint32_t* __restrict__ status, int stages, int tmem_cols, QuantPassOut qo) {
@@ -308,6 +317,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 1) k_amax_lora(
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(abort_flag + 1);
+  float* inv_tab = reinterpret_cast<float*>(smem + stages * stage_bytes + 256);   // QUANT: 256 floats
 
   constexpr int kWorkers = lora_workers<QUANT>();
   constexpr int kThreads = lora_threads<QUANT>();
@@ -351,6 +361,8 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 1) k_amax_lora(
     ts = __fdiv_rn(m, 2688.0f);
     if (ts == 0.0f) ts = 1.0f;
     if (blockIdx.x == 0 && threadIdx.x == 0) *qo.ts_out = ts;
+    if (threadIdx.x < 256) inv_tab[threadIdx.x] = block_inv(ts, threadIdx.x);
+    __syncthreads();
   }
 
   if (warp == 0) {
@@ -426,7 +438,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 1) k_amax_lora(
     // scales are loaded one stage ahead
     const int qj = at & 3, qr = at >> 2;
     const unsigned gmask = 0xFu << (lane & 28);
-    const QuantCtx qc{ts, __fmul_rn(6.0f, ts), K >> 4, K, qo.codes, qo.scales};
+    const QuantCtx qc{ts, __fmul_rn(6.0f, ts), K >> 4, K, qo.codes, qo.scales, inv_tab};
     float qs_next[16];
     if (QUANT) load_scale16(pqs, qj, qs_next);
     // The per-channel scales of a stage are loaded two stages ahead: the
@@ -607,15 +619,22 @@ static cudaError_t launch_lora_pass(const CUtensorMap& tm_x, const CUtensorMap& 
                                     int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
                                     int sm_count, const QuantPassOut& qo, int* grid_out, cudaStream_t st) {
   const int stage_bytes = 16384 + rank * 128;
-  constexpr int kSmemLimit = 232448;
-  int stages = (kSmemLimit - 1024 - 256) / stage_bytes;
-  if (stages > 8) stages = 8;
-  if (stages < 2) return cudaErrorInvalidValue;
-  const int smem = stages * stage_bytes + 1024 + 256;
+  constexpr int kSmemLimit = 232448;     // per CTA, one CTA per SM
+  constexpr int kSmemPerSm = 233472;     // shared memory of an SM (228 KB), 1 KB of it reserved per CTA
+  const int tail = 256 + (QUANT ? 1024 : 0);   // barriers, flags, partial maxima (+ reciprocal table)
   int tmem_cols = 32;
   while (tmem_cols < rank) tmem_cols <<= 1;
+  // two CTAs per SM when their accumulators fit TMEM together and each gets a
+  // ring of at least 3 stages; else one CTA with up to 8 stages
+  const int two_stages = (kSmemPerSm / 2 - 1024 - 1024 - tail) / stage_bytes;
+  const bool two = (QUANT || kLoraAmaxTwoCtas) && 2 * tmem_cols <= 512 && two_stages >= 3;
+  int stages = two ? two_stages : (kSmemLimit - 1024 - tail) / stage_bytes;
+  if (stages > 8) stages = 8;
+  if (stages < 2) return cudaErrorInvalidValue;
+  const int smem = stages * stage_bytes + 1024 + tail;
   const int tiles = (M + 127) / 128;
-  int grid = tiles < sm_count ? tiles : sm_count;
+  const int slots = (two ? 2 : 1) * sm_count;
+  int grid = tiles < slots ? tiles : slots;
   if (grid > kMaxPartials) grid = kMaxPartials;
   cudaError_t e = cudaFuncSetAttribute(k_amax_lora<QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
