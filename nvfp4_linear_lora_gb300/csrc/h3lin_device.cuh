@@ -261,6 +261,16 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8]) {
   return out;
 }
 
+// (r0, r1) = (a0 * b0, a1 * b1), each rounded to nearest even: one packed
+// f32x2 multiply on sm_100+ (the same results as two __fmul_rn).
+__device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Byte offset of the scale of (row, 16-block j) in the native scale layout.
 __host__ __device__ __forceinline__ int64_t sf_offset(int64_t row, int64_t j, int64_t K) {
   const int64_t atom = (row >> 7) * (K >> 6) + (j >> 2);

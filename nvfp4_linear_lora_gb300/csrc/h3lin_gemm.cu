@@ -371,6 +371,15 @@ __device__ __forceinline__ float silu_mul_fast(float scale, uint32_t acc_g, uint
   const float u = __fmul_rn(scale, __uint_as_float(acc_u));
   return __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
 }
+// The same for two adjacent columns, the multiplies paired (identical results;
+// the epilogue's instruction count shows up in the MMA issue rate).
+__device__ __forceinline__ uint32_t silu_mul2_bf16(float scale, uint32_t g0, uint32_t g1, uint32_t u0, uint32_t u1) {
+  float ga, gb, ua, ub, oa, ob;
+  fmul2_rn(__uint_as_float(g0), __uint_as_float(g1), scale, scale, ga, gb);
+  fmul2_rn(__uint_as_float(u0), __uint_as_float(u1), scale, scale, ua, ub);
+  fmul2_rn(__fdividef(ga, 1.0f + __expf(-ga)), __fdividef(gb, 1.0f + __expf(-gb)), ua, ub, oa, ob);
+  return pack_bf16x2(oa, ob);
+}
 
 // The warp's staging block (32 rows x 64 bytes, 16-byte chunks placed as the
 // 64-byte TMA swizzle lays them out) -> global through the TMA engine; rows
@@ -650,11 +659,13 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
             w[k] = SILU ? __float_as_uint(silu_mul_fast(scale, a[c], b[c]))
                         : __float_as_uint(__fmul_rn(scale, __uint_as_float(c < 32 ? a[c] : b[c - 32])));
           } else if (SILU) {
-            w[k] = pack_bf16x2(silu_mul_fast(scale, a[2 * k], b[2 * k]), silu_mul_fast(scale, a[2 * k + 1], b[2 * k + 1]));
+            w[k] = silu_mul2_bf16(scale, a[2 * k], a[2 * k + 1], b[2 * k], b[2 * k + 1]);
           } else {
             const int c = rd * 32 + 2 * k;
             const uint32_t lo = c < 32 ? a[c] : b[c - 32], hi = c < 32 ? a[c + 1] : b[c - 31];
-            w[k] = pack_bf16x2(__fmul_rn(scale, __uint_as_float(lo)), __fmul_rn(scale, __uint_as_float(hi)));
+            float ylo, yhi;
+            fmul2_rn(__uint_as_float(lo), __uint_as_float(hi), scale, scale, ylo, yhi);
+            w[k] = pack_bf16x2(ylo, yhi);
           }
         }
         if (AMAX && row0 + lane < M) {

@@ -35,16 +35,6 @@ __device__ __forceinline__ void load_scale8(const float* __restrict__ pqs, int c
   }
 }
 
-// (r0, r1) = (a0 * b0, a1 * b1), each rounded to nearest even: one packed
-// f32x2 multiply on sm_100+ (the same results as two __fmul_rn).
-__device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
-  asm("{\n\t.reg .b64 a, b, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(r0), "=f"(r1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
 __device__ __forceinline__ void prescale8(const uint4& w, const float (&s)[8], float (&v)[8]) {
   fmul2_rn(bf16lo(w.x), bf16hi(w.x), s[0], s[1], v[0], v[1]);
   fmul2_rn(bf16lo(w.y), bf16hi(w.y), s[2], s[3], v[2], v[3]);
