@@ -36,9 +36,9 @@ from nvfp4_linear_lora_gb300 import configs, synth  # noqa: E402
 # profiles/dram_fp4gemm_pair_S37726.md.  It is reported only while the GEMM
 # sources hash to the value the capture was taken with; after any change to
 # them the counters no longer describe the kernel and `traffic` is null.
-GEMM_TRAFFIC = {"sources_sha256": "2d6443229f9444a0a1d1f0f5a80c6a7f1b8dfc3a3cd770c9f94306580b14982c", "S": 37726,
-                "bytes_per_launch": {"qkv": 509207040 + 1118639616, "attn_out": 135006720 + 338439424,
-                                     "gate_up": 558959104 + 1007155968, "down": 560922112 + 368015872}}
+GEMM_TRAFFIC = {"sources_sha256": "81cd8c5729a09808481d11bba2a1b1abcf6cc88fa163e8dbbc11e1ad7ce9306b", "S": 37726,
+                "bytes_per_launch": {"qkv": 501951488 + 1118704128, "attn_out": 134770176 + 338481920,
+                                     "gate_up": 558524672 + 1007130624, "down": 548595712 + 367817984}}
 GEMM_SOURCES = ("nvfp4_linear_lora_gb300/csrc/h3lin_gemm.cu", "nvfp4_linear_lora_gb300/csrc/h3lin_device.cuh")
 
 
