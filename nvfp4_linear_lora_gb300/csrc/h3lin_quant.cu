@@ -122,11 +122,26 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict_
 // (never split across rows, K % 64 == 0) assemble the 32-bit scale word.
 struct QuantCtx {
   float ts, six_ts;
-  int kb, K;
-  uint2* codes;      // 8 bytes = 16 codes per block
-  uint8_t* scales;
+  float rcp_six_ts;       // fl(1 / six_ts)
   const float* inv_tab;   // optional: 1 / (E4M3(sb) * ts) for every scale byte sb (shared memory)
 };
+__device__ __forceinline__ QuantCtx make_quant_ctx(float ts, const float* inv_tab) {
+  const float six_ts = __fmul_rn(6.0f, ts);
+  return QuantCtx{ts, six_ts, __frcp_rn(six_ts), inv_tab};
+}
+
+// sb = E4M3_sat(fl(bm / (6 ts))), mostly without the division: p = fl(bm *
+// fl(1 / (6 ts))) lies within 2.5 ulp of the exact quotient, so p and the
+// IEEE quotient are at most 2 ulp apart and round to the same E4M3 value
+// unless an E4M3 rounding midpoint (float mantissa bit 19 set, bits 18-0
+// clear) is within 3 ulp of p, or p is below 2^-6 (E4M3's subnormal range,
+// where the midpoints sit elsewhere).  Only those cases take the division.
+__device__ __forceinline__ uint32_t block_scale_byte(float bm, const QuantCtx& q) {
+  const float p = __fmul_rn(bm, q.rcp_six_ts);
+  const uint32_t low = __float_as_uint(p) & 0xFFFFFu;
+  if (p < 0x1p-6f || low - (0x80000u - 3u) <= 6u) return e4m3_rn_satfinite(__fdiv_rn(bm, q.six_ts));
+  return e4m3_rn_satfinite(p);
+}
 
 // inv_tab[sb] = 1 / fl(E4M3(sb) * ts), the same two roundings quant_block takes
 // per block, tabulated once per CTA for the 256 scale bytes.
@@ -148,10 +163,11 @@ __device__ __forceinline__ void load_scale16(const float* __restrict__ pqs, int 
   }
 }
 
-// Quantise one 16-element block (two 16-byte halves) of row `row`.
-// The block's codes are stored only when write_codes (rows >= M have none).
-__device__ __forceinline__ void quant_block(const QuantCtx& q, int row, int b, const uint4& w0, const uint4& w1,
-                                            const float (&s)[16], unsigned gmask, int lane, bool write_codes = true) {
+// Quantise one 16-element block (two 16-byte halves): its 16 codes go to
+// *code (skipped when code is null: rows >= M have none) and its scale byte
+// to *sf (each thread writes its own byte of the row's 4-byte scale word).
+__device__ __forceinline__ void quant_block(const QuantCtx& q, uint2* code, uint8_t* sf, const uint4& w0,
+                                            const uint4& w1, const float (&s)[16]) {
   float v[16];
   {
     float h0[8], h1[8], s0[8], s1[8];
@@ -165,7 +181,7 @@ __device__ __forceinline__ void quant_block(const QuantCtx& q, int row, int b, c
   float bm = fabsf(v[0]);
 #pragma unroll
   for (int i = 1; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
-  const uint32_t sb = e4m3_rn_satfinite(__fdiv_rn(bm, q.six_ts));
+  const uint32_t sb = block_scale_byte(bm, q);
   const float inv = q.inv_tab ? q.inv_tab[sb] : block_inv(q.ts, sb);
   float qa[8], qb[8];
 #pragma unroll
@@ -173,19 +189,15 @@ __device__ __forceinline__ void quant_block(const QuantCtx& q, int row, int b, c
     fmul2_rn(v[i], v[i + 1], inv, inv, qa[i], qa[i + 1]);
     fmul2_rn(v[8 + i], v[9 + i], inv, inv, qb[i], qb[i + 1]);
   }
-  uint2 code = make_uint2(0u, 0u);
-  if (isfinite(inv)) code = make_uint2(e2m1x8(qa), e2m1x8(qb));
-  if (write_codes) q.codes[static_cast<int64_t>(row) * q.kb + b] = code;
-  const uint32_t s1 = __shfl_down_sync(gmask, sb, 1, 4);
-  const uint32_t s2 = __shfl_down_sync(gmask, sb, 2, 4);
-  const uint32_t s3 = __shfl_down_sync(gmask, sb, 3, 4);
-  if ((lane & 3) == 0)
-    *reinterpret_cast<uint32_t*>(q.scales + sf_offset(row, b, q.K)) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  uint2 cw = make_uint2(0u, 0u);
+  if (isfinite(inv)) cw = make_uint2(e2m1x8(qa), e2m1x8(qb));
+  if (code) *code = cw;
+  *sf = static_cast<uint8_t>(sb);
 }
 
 // Rows are visited from the last to the first: the amax pass streamed them
 // in ascending order, so the tail of x is still in L2 when this pass starts.
-__global__ void __launch_bounds__(kQuantThreads) k_quant(
+__global__ void __launch_bounds__(kQuantThreads, 4) k_quant(
     const uint4* __restrict__ x, int M, int Mpad, int K, const float* __restrict__ pqs,
     const float* __restrict__ partials, int nparts, const int* __restrict__ nparts_dev, uint2* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ ts_out, int rows_step, const uint4* __restrict__ b_src,
@@ -199,13 +211,11 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant(
   if (ts == 0.0f) ts = 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
   const int kb = K >> 4;
-  QuantCtx q{ts, __fmul_rn(6.0f, ts), kb, K, codes, scales, nullptr};
+  const QuantCtx q = make_quant_ctx(ts, nullptr);
 
   const int tid = blockIdx.x * kQuantThreads + threadIdx.x;
   const int b = tid % kb;
   const int r0 = tid / kb;
-  const int lane = threadIdx.x & 31;
-  const unsigned gmask = 0xFu << (lane & 28);
   const int kc = K >> 3;   // 16-byte chunks per row
   if (r0 < rows_step) {
     float s[16];
@@ -225,17 +235,11 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant(
         c0 = __ldcs(p);
         c1 = __ldcs(p + 1);
       }
-      if (ra < M) {
-        quant_block(q, ra, b, a0, a1, s, gmask, lane);
-      } else if ((lane & 3) == 0) {
-        *reinterpret_cast<uint32_t*>(scales + sf_offset(ra, b, K)) = 0u;
-      }
+      if (ra < M) quant_block(q, codes + static_cast<int64_t>(ra) * kb + b, scales + sf_offset(ra, b, K), a0, a1, s);
+      else scales[sf_offset(ra, b, K)] = 0;
       if (has_b) {
-        if (rb < M) {
-          quant_block(q, rb, b, c0, c1, s, gmask, lane);
-        } else if ((lane & 3) == 0) {
-          *reinterpret_cast<uint32_t*>(scales + sf_offset(rb, b, K)) = 0u;
-        }
+        if (rb < M) quant_block(q, codes + static_cast<int64_t>(rb) * kb + b, scales + sf_offset(rb, b, K), c0, c1, s);
+        else scales[sf_offset(rb, b, K)] = 0;
       }
     }
   }
@@ -427,8 +431,17 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     // QUANT: block qj of rows qr + kQuantRowStep h of each stage; its 16
     // scales are loaded one stage ahead
     const int qj = at & 3, qr = at >> 2;
-    const unsigned gmask = 0xFu << (lane & 28);
-    const QuantCtx qc{ts, __fmul_rn(6.0f, ts), K >> 4, K, qo.codes, qo.scales, inv_tab};
+    const QuantCtx qc = make_quant_ctx(ts, inv_tab);
+    constexpr int kQuantRowStep = 8 * kWorkers;       // rows covered by the workers at once
+    constexpr int kQuantRows = 128 / kQuantRowStep;   // rows of a tile per thread
+    // byte offset of block qj of each of this thread's rows inside a 512-byte
+    // scale atom (the native layout: (r % 32) * 16 + (r / 32) * 4 + j)
+    int sf_in_atom[kQuantRows];
+#pragma unroll
+    for (int h = 0; h < kQuantRows; ++h) {
+      const int r = qr + kQuantRowStep * h;
+      sf_in_atom[h] = (r & 31) * 16 + (r >> 5) * 4 + qj;
+    }
     float qs_next[16];
     if (QUANT) load_scale16(pqs, qj, qs_next);
     // The per-channel scales of a stage are loaded two stages ahead: the
@@ -439,6 +452,18 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
       load_scale8(pqs, (nk > 1 ? 1 : 0) * 8 + ch, s1);
     }
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      // QUANT: the tile's scale atoms start at sf_tile (one per 64 columns);
+      // row h's codes at code_row[h] (null past M: rows >= M get no codes)
+      uint8_t* sf_tile = nullptr;
+      uint2* code_row[kQuantRows];
+      if (QUANT) {
+        sf_tile = qo.scales + static_cast<int64_t>(t) * (K >> 6) * 512;
+#pragma unroll
+        for (int h = 0; h < kQuantRows; ++h) {
+          const int row = t * 128 + qr + kQuantRowStep * h;
+          code_row[h] = row < M ? qo.codes + static_cast<int64_t>(row) * (K >> 4) + qj : nullptr;
+        }
+      }
       for (int kc = 0; kc < nk; ++kc) {
         if (QUANT) {
           float qs[16];
@@ -448,15 +473,14 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
           load_scale16(pqs, 4 * kn + qj, qs_next);
           if (!mbar_wait(&full[st], ph, ab)) goto amax_done;
           const uint8_t* tile = smem + st * stage_bytes;
-          constexpr int kQuantRowStep = 8 * kWorkers;   // rows covered by the workers at once
 #pragma unroll
-          for (int h = 0; h < 128 / kQuantRowStep; ++h) {
+          for (int h = 0; h < kQuantRows; ++h) {
             const int r = qr + kQuantRowStep * h;
-            const int row = t * 128 + r;
             const uint4 w0 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj) ^ (r & 7)) << 4));
             const uint4 w1 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj + 1) ^ (r & 7)) << 4));
-            // rows >= M were filled with zeros by the TMA load: scale word 0, no codes
-            quant_block(qc, row, 4 * kc + qj, w0, w1, qs, gmask, lane, row < M);
+            // rows >= M were filled with zeros by the TMA load: scale 0, no codes
+            quant_block(qc, code_row[h] ? code_row[h] + 4 * kc : nullptr, sf_tile + kc * 512 + sf_in_atom[h], w0, w1,
+                        qs);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[st]);
