@@ -11,8 +11,11 @@
 // HBM-bound: 2 B read + 2 B written per element.  One row per CTA iteration
 // (128 threads, grid-strided, many CTAs per SM): a thread keeps its
 // 16-byte chunks c = t + 128 j of the row in registers across the two
-// block reductions (mean, then the centred sum of squares); the table row and
-// the per-channel scales are small and re-read through L1.
+// block reductions (mean, then the centred sum of squares); the table row is
+// small and re-read through L1.  The amax needs no per-element multiply: a
+// thread keeps the column-wise max |x_mod| of its chunks (packed bf16) and
+// scales it by |s_next| once at the end, which is exact because rounding is
+// monotone: max_r |fl(h_r * s)| = fl(max_r |h_r| * |s|).
 #include "h3lin_device.cuh"
 
 namespace h3lin {
@@ -50,7 +53,11 @@ __global__ void __launch_bounds__(kModThreads) k_modulate(const uint4* __restric
   __shared__ float red[kModThreads / 32];
   const int kc = K >> 3;
   const float inv_k = 1.0f / static_cast<float>(K);
-  float am = 0.0f;
+  __nv_bfloat162 colmax[CPT][4];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) colmax[j][k] = __float2bfloat162_rn(0.0f);
   for (int row = blockIdx.x; row < M; row += gridDim.x) {
     uint4 w[CPT];
     float s = 0.0f;
@@ -106,20 +113,31 @@ __global__ void __launch_bounds__(kModThreads) k_modulate(const uint4* __restric
         const uint4 r = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                                    pack_bf16x2(o[6], o[7]));
         out[int64_t(row) * kc + c] = r;
-        // amax of the stored bf16 values times the consumer's per-channel scale
-        float ps[8] = {1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f};
-        if (pqs) {
-          const float4 p0 = __ldg(reinterpret_cast<const float4*>(pqs) + 2 * c);
-          const float4 p1 = __ldg(reinterpret_cast<const float4*>(pqs) + 2 * c + 1);
-          ps[0] = p0.x; ps[1] = p0.y; ps[2] = p0.z; ps[3] = p0.w;
-          ps[4] = p1.x; ps[5] = p1.y; ps[6] = p1.z; ps[7] = p1.w;
-        }
         const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          am = fmaxf(am, fabsf(__fmul_rn(bf16lo(rw[k]), ps[2 * k])));
-          am = fmaxf(am, fabsf(__fmul_rn(bf16hi(rw[k]), ps[2 * k + 1])));
-        }
+        for (int k = 0; k < 4; ++k)
+          colmax[j][k] = __hmax2(colmax[j][k], __habs2(*reinterpret_cast<const __nv_bfloat162*>(&rw[k])));
+      }
+    }
+  }
+  // amax of the stored bf16 values times the consumer's per-channel scale
+  float am = 0.0f;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + kModThreads * j;
+    if (c < kc) {
+      float ps[8] = {1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f};
+      if (pqs) {
+        const float4 p0 = __ldg(reinterpret_cast<const float4*>(pqs) + 2 * c);
+        const float4 p1 = __ldg(reinterpret_cast<const float4*>(pqs) + 2 * c + 1);
+        ps[0] = p0.x; ps[1] = p0.y; ps[2] = p0.z; ps[3] = p0.w;
+        ps[4] = p1.x; ps[5] = p1.y; ps[6] = p1.z; ps[7] = p1.w;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(&colmax[j][k]);
+        am = fmaxf(am, __fmul_rn(bf16lo(u), fabsf(ps[2 * k])));
+        am = fmaxf(am, __fmul_rn(bf16hi(u), fabsf(ps[2 * k + 1])));
       }
     }
   }
