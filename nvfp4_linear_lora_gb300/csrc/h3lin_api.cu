@@ -92,8 +92,8 @@ bool make_sf_map(CUtensorMap* m, const void* base, uint64_t bytes) {
   return r == CUDA_SUCCESS;
 }
 
-// Output [rows, cols] (bf16 or fp32) stored by 32-row x 128-byte boxes,
-// 128-byte swizzle (the epilogue's staging layout).
+// Output [rows, cols] (bf16 or fp32) stored by 32-row x 64-byte boxes,
+// 64-byte swizzle (the epilogue's staging layout).
 bool make_out_map(CUtensorMap* m, void* base, bool f32, int64_t cols, int64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
