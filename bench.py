@@ -684,6 +684,23 @@ def native_arm(a, rank, world, local_rank):
         cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cpu_info(), "kind": "oracle",
                "sample": f"{m} rows x {n} output columns of each projection (same S={S} workload), {t:.1f} s"}
 
+    # the base-only fraction of the FP4 peak and the BF16-peak fraction of the
+    # LoRA part: the merged-LoRA block does the same base work with no LoRA
+    # branch, and the dynamic block's extra time is what its A(x) and B(u) cost
+    split = None
+    if merged_line is not None:
+        mms = merged_line["ms_per_block"]
+        lora_ms = ms - mms
+        lora_tf = (ldown + lup) / (lora_ms * 1e-3) / 1e12 if lora_ms > 0 else None
+        split = {"base_only": {"ms_per_block": mms, "tflops": world * base / (mms * 1e-3) / 1e12,
+                               "frac_of_fp4_peak": base / (mms * 1e-3) / 1e12 / peak_fp4},
+                 "lora_part": {"ms_per_block": lora_ms, "tflops": None if lora_tf is None else world * lora_tf,
+                               "frac_of_bf16_peak": None if lora_tf is None else lora_tf / peak_bf16},
+                 "how": "base only = the block with every adapter merged into its weight (merged_lora: the same "
+                        "base work, no LoRA branch); LoRA part = the dynamic block's extra time over it, for the "
+                        "A(x) and B(u) FLOPs (a marginal cost: A(x) runs inside the HBM-bound amax pass, where "
+                        "it partly hides, so this fraction can exceed 1); peaks as in frac_of_fp4_peak and roofline"}
+
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e2m1+bf16", "data": "synthetic",
@@ -695,7 +712,7 @@ def native_arm(a, rank, world, local_rank):
             "ms_per_block": ms, "frac_of_fp4_peak": value / world / peak_fp4,
             "flops_per_block": {"total": total, "base_fp4": base, "lora_down": ldown, "lora_up": lup},
             "kernel_ms": {"gemm": gemm_total_ms, "prepare": ms - gemm_total_ms},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "merged_lora": merged_line,
+            "roofline": roofline, "peak_split": split, "cpu_baseline": cpu, "e2e": e2e, "merged_lora": merged_line,
             "qk_norm_rope": rope_line, "modulation": mod_line,
             "gpu_launches": blk.launches_per_step() * a.steps, "clocks": clocks,
             "peaks": {"kind": peak_kind, **peaks}}
