@@ -252,3 +252,16 @@ def test_native_scale_layout_is_a_bijection():
         off = native_scale_offsets(rows, K).reshape(-1)
         assert len(set(off.tolist())) == off.size
         assert off.max() < h3lin.h3lin_scales_bytes(rows, K)
+
+
+def test_noalloc_host_checks():
+    # the allocation-free forward refuses work beyond its fixed scratch, and a
+    # missing weight, on the host: before it looks up any device
+    K, N = 5120, 15360
+    M = 1 + h3lin.H3LIN_NOALLOC_SCRATCH_BYTES // (K // 2)
+    w = h3lin.h3lin_weight(A, A, A, N, K)
+    assert h3lin.h3lin_forward_noalloc(A, M, None, w, 0, None, 1.0, A, 0, None) == h3lin.H3LIN_E_WORKSPACE
+    assert h3lin.h3lin_forward_noalloc(A, 16, None, None, 0, None, 1.0, A, 0, None) == h3lin.H3LIN_E_INVALID
+    # the projection the GPU test of this entry point runs fits in the scratch
+    fits = h3lin.h3lin_forward_workspace_bytes(1024, 1024, 1280, 128)
+    assert 0 < fits <= h3lin.H3LIN_NOALLOC_SCRATCH_BYTES
