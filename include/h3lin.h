@@ -364,19 +364,31 @@ h3lin_status h3lin_selftest_wait_timeout(void* workspace, size_t workspace_bytes
  * cudaFree are forbidden because they can block on the device).  Same
  * arguments and results as h3lin_forward, minus the workspace: the scratch
  * is a fixed H3LIN_NOALLOC_SCRATCH_BYTES array inside the library, one per
- * device, held from module load until process exit.  Nothing is allocated.
+ * CUDA context the library's module is loaded into, held until that context
+ * is destroyed (the primary context: process exit or cudaDeviceReset).
+ * Nothing is allocated.
  *   - Calls whose scratch need (h3lin_forward_workspace_bytes) exceeds
  *     H3LIN_NOALLOC_SCRATCH_BYTES return H3LIN_E_WORKSPACE, enqueueing nothing.
- *   - All calls on a device share the array; calls that may overlap on the
+ *   - All calls in a context share the array; calls that may overlap on the
  *     GPU race on it.  Order them on one stream.
- *   - The first call on each device looks up the array's device address;
- *     make it before any stream capture begins.
- *   - The device status word is internal to the array (not readable). */
+ *   - The array's device address is looked up on the first call made in each
+ *     context (the current one) and again whenever a call finds a context it
+ *     has not seen before, e.g. after cudaDeviceReset or when the caller makes
+ *     its own driver context current.  Make the first call in each context
+ *     before any stream capture begins.
+ *   - A timed-out device wait is recorded in a status word inside the array,
+ *     not returned by this call (which only enqueues): read it, and clear it,
+ *     with h3lin_noalloc_read_status. */
 #define H3LIN_NOALLOC_SCRATCH_BYTES (64u << 20)
 h3lin_status h3lin_forward_noalloc(const void* x, int64_t M, const float* pre_quant_scale,
                                    const h3lin_weight* weight, int32_t epilogue,
                                    const h3lin_adapter* adapter, float strength, void* out,
                                    int32_t out_dtype, cudaStream_t stream);
+/* Synchronises `stream`, reads the status word of the current context's
+ * allocation-free scratch into *device_status (H3LIN_OK or H3LIN_E_TIMEOUT)
+ * and, when it is set, clears it so that later calls start clean.  No
+ * counterpart in the paper.  Allocates nothing. */
+h3lin_status h3lin_noalloc_read_status(cudaStream_t stream, int32_t* device_status);
 
 /* ------------------------------------------------------------------ status */
 /* Synchronises `stream`, then reads the workspace's sticky device status word

@@ -85,6 +85,7 @@ _SIGNATURES = {
     "h3lin_merge_lora": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(h3lin_adapter), _f32, _vp, _vp]),
     "h3lin_forward_noalloc": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), _i32,
                                      ctypes.POINTER(h3lin_adapter), _f32, _vp, _i32, _vp]),
+    "h3lin_noalloc_read_status": (_i32, [_vp, ctypes.POINTER(_i32)]),
 }
 
 H3LIN_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -202,6 +203,14 @@ def h3lin_forward_noalloc(x, M, pqs, weight, epilogue, adapter, strength, out, o
     wp = ctypes.byref(weight) if weight is not None else None
     ap = ctypes.byref(adapter) if adapter is not None else None
     return lib().h3lin_forward_noalloc(x, M, pqs, wp, epilogue, ap, strength, out, out_dtype, stream)
+
+
+def h3lin_noalloc_read_status(stream):
+    """(call status, device status word of the allocation-free scratch); a set
+    word is cleared by the read."""
+    v = _i32(-1)
+    st = lib().h3lin_noalloc_read_status(stream, ctypes.byref(v))
+    return st, v.value
 
 
 def h3lin_merge_lora(w, N, K, pqs, adapter, strength, w_out, stream):

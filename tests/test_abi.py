@@ -262,6 +262,8 @@ def test_noalloc_host_checks():
     w = h3lin.h3lin_weight(A, A, A, N, K)
     assert h3lin.h3lin_forward_noalloc(A, M, None, w, 0, None, 1.0, A, 0, None) == h3lin.H3LIN_E_WORKSPACE
     assert h3lin.h3lin_forward_noalloc(A, 16, None, None, 0, None, 1.0, A, 0, None) == h3lin.H3LIN_E_INVALID
+    # its status read needs somewhere to put the word (checked before any device call)
+    assert h3lin.lib().h3lin_noalloc_read_status(None, None) == h3lin.H3LIN_E_INVALID
     # the projection the GPU test of this entry point runs fits in the scratch
     fits = h3lin.h3lin_forward_workspace_bytes(1024, 1024, 1280, 128)
     assert 0 < fits <= h3lin.H3LIN_NOALLOC_SCRATCH_BYTES
