@@ -22,16 +22,21 @@ in their plainest reading:
              when that quotient is zero).
 
 Every floating-point step that decides a code is carried out in IEEE float32
-with round-to-nearest-even, in exactly this order (the same order the GPU
-kernel uses, so that both take the integer decision in the same precision):
+with round-to-nearest-even, in exactly this order (so that the GPU kernels,
+which take the same integer decisions in float32, can be compared bit for
+bit):
 
 1. ``v = x * s``                        pre_quant_scale ``s`` (absent -> 1)
 2. ``amax = max |v|`` over the tensor, ``ts = amax / 2688`` (0 -> 1)
 3. per 16-block: ``bamax = max |v|``; ``sb = E4M3_rne_sat(bamax / (6 * ts))``
-4. ``d = decode(sb) * ts``; ``inv_d = 1 / d``
-5. ``q = v * inv_d``; ``code = E2M1_rne_sat(q)`` with the sign of ``q`` kept
-   (a negative value that rounds to zero gives code 0x8).  A block whose
-   ``inv_d`` is not finite (``d == 0``) gets all-zero codes.
+4. ``d = decode(sb) * ts``
+5. ``q = v / d`` (the IEEE float32 quotient); ``code = E2M1_rne_sat(q)`` with
+   the sign of ``q`` kept (a negative value that rounds to zero gives code
+   0x8).  A block with ``d == 0`` gets all-zero codes.
+
+Step 5 is the plain definition of an element's code, the quotient of the
+value by its block's dequantisation scale, rounded once to float32; nothing
+on the pages asks for another order of operations.
 """
 from __future__ import annotations
 
@@ -149,10 +154,9 @@ def quantize_blocks(v, ts):
     six_ts = np.float32(6.0) * ts                              # float32 RN
     sb = e4m3_encode(bamax / six_ts)                           # float32 RN division
     d = e4m3_decode(sb).astype(np.float32) * ts                # float32 RN
-    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
-        inv_d = np.float32(1.0) / d                            # float32 RN
-        q = blk * inv_d[:, :, None]                            # float32 RN
-    ok = np.isfinite(inv_d)
+    ok = d != 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = blk / np.where(ok, d, np.float32(1.0))[:, :, None]  # float32 RN division
     q = np.where(ok[:, :, None], q, np.float32(0.0)).astype(np.float32)
     codes = e2m1_encode(q)
     codes = np.where(ok[:, :, None], codes, np.uint8(0)).astype(np.uint8)

@@ -175,8 +175,37 @@ def test_zero_block_all_zero_codes():
 
 
 # ------------------------------------------------------------------ brute-force quantise
+def _f32_rn(q):
+    """The float32 nearest to the exact rational q (ties to the even
+    significand), from the binary representation: significand rounded at 24
+    bits, or at 2^-149 in the subnormal range.  No float division involved."""
+    if q == 0:
+        return np.float32(0.0)
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()      # 2^e <= a < 2^(e+2)
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    step = Fraction(2) ** max(e - 23, -149)                         # one unit in the last place
+    m = round(a / step)                                             # Fraction.__round__: half to even
+    val = float(m * step)                                           # exact: at most 25 significant bits
+    return np.float32(-val if q < 0 else val)
+
+
+def test_f32_rn_matches_ieee_division_on_random_pairs():
+    # the helper against the IEEE float32 division numpy performs
+    rng = np.random.default_rng(21)
+    a = (rng.standard_normal(3000) * np.exp2(rng.uniform(-60, 60, 3000))).astype(np.float32)
+    b = np.abs(rng.standard_normal(3000) * np.exp2(rng.uniform(-60, 60, 3000))).astype(np.float32) + np.float32(1e-30)
+    want = a / b
+    got = np.array([_f32_rn(Fraction(float(x)) / Fraction(float(y))) for x, y in zip(a, b)], dtype=np.float32)
+    np.testing.assert_array_equal(got, want)
+
+
 def _quantize_bruteforce(x, s):
-    """Element-by-element quantisation with exhaustive nearest-value searches."""
+    """Element-by-element quantisation with exhaustive nearest-value searches;
+    each code from the exact quotient v / d rounded once to float32."""
     M, K = x.shape
     f32 = np.float32
     v = [[f32(x[m, k]) * f32(s[k]) for k in range(K)] for m in range(M)]
@@ -200,14 +229,67 @@ def _quantize_bruteforce(x, s):
             d = f32(sval) * ts
             if d == 0:
                 continue
-            inv = f32(1.0) / d
             for i, t in enumerate(blk):
-                codes[m, 16 * b + i] = _e2m1_brute(f32(t) * inv)
+                q = _f32_rn(Fraction(float(t)) / Fraction(float(d)))
+                if q == 0 and np.signbit(f32(t)):
+                    q = f32(-0.0)
+                codes[m, 16 * b + i] = _e2m1_brute(q)
     packed = np.zeros((M, K // 2), dtype=np.uint8)
     for m in range(M):
         for j in range(K // 2):
             packed[m, j] = codes[m, 2 * j] | (codes[m, 2 * j + 1] << 4)
     return packed, scales, ts
+
+
+def test_codes_follow_the_quotient_where_the_reciprocal_product_differs():
+    """Blocks built so that fl(v * fl(1/d)) and fl(v / d) fall on different
+    sides of an E2M1 rounding midpoint: quantize_blocks must give the code of
+    the exact quotient rounded once (brute force), not the product's."""
+    f32 = np.float32
+    rng = np.random.default_rng(31)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    ks = nvfp4.e4m3_decode(np.arange(0x30, 0x48, dtype=np.uint8))     # E4M3 values 0.5 .. 4.5
+    found = []
+    for _ in range(400000):
+        k = f32(rng.choice(ks))
+        ts = f32(rng.uniform(0.5, 2.0))
+        d = f32(k * ts)
+        v = f32(f32(rng.choice(mids)) * d)
+        for step in range(-3, 4):   # walk v across the midpoint
+            vv = v
+            for _ in range(abs(step)):
+                vv = np.nextafter(vv, f32(np.inf) if step > 0 else f32(0.0))
+            if nvfp4.e2m1_encode(vv / d) != nvfp4.e2m1_encode(vv * (f32(1.0) / d)):
+                found.append((k, ts, d, vv))
+        if len(found) >= 8:
+            break
+    assert found, "no element whose code depends on the reading"
+    for k, ts, d, vv in found:
+        row = np.zeros((1, 16), dtype=np.float32)
+        row[0, 0] = f32(f32(6.0) * d)             # block max: scale byte k, so the block's d is fl(k * ts)
+        row[0, 1] = vv
+        row[0, 2] = -vv
+        codes, sb = nvfp4.quantize_blocks(row, ts)
+        assert nvfp4.e4m3_decode(sb[0, 0]) == k
+        for i in (1, 2):
+            want = _e2m1_brute(_f32_rn(Fraction(float(row[0, i])) / Fraction(float(d))))
+            assert codes[0, i] == want
+
+
+def test_tiny_blocks_quantise_by_the_quotient():
+    """Tensor scales so small that 1/d overflows float32 (d < 2^-128): the
+    codes still follow v / d (they are not all zero)."""
+    x = np.zeros((2, 32), dtype=np.float32)
+    x[0, :16] = np.float32(2.0 ** -130) * np.arange(1, 17, dtype=np.float32)
+    x[1, 16:] = -np.float32(2.0 ** -128) * np.arange(16, 0, -1, dtype=np.float32)
+    pq, sc, ts = nvfp4.quantize(x, None)
+    bq, bsc, bts = _quantize_bruteforce(x, np.ones(32, dtype=np.float32))
+    assert ts == bts and ts < 2.0 ** -130
+    np.testing.assert_array_equal(sc, bsc)
+    np.testing.assert_array_equal(pq, bq)
+    d0 = np.float32(nvfp4.e4m3_decode(sc[0, 0])) * ts
+    assert d0 < 2.0 ** -128 and not np.isfinite(np.float32(1.0) / d0)
+    assert np.any(pq[0, :8] != 0)
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
