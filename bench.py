@@ -63,6 +63,7 @@ def gemm_algorithmic_bytes(S):
 
 METRIC = "NVFP4+LoRA projection TFLOP/s at S=37726 (% of dense FP4 peak); ms/block"
 FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor ratio on GB300
+FP4_NOMINAL_TFLOPS = 13500.0      # GB300 datasheet dense FP4 (no sparsity), for context next to the measured-derived peak
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -83,6 +84,10 @@ def parse_args(argv=None):
                     help="skip the modulation-producer measurement on the block's QKV input")
     ap.add_argument("--no-rope", action="store_true",
                     help="skip the Q/K RMSNorm + RoPE measurement on the block's QKV output")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the sequence-length sweep of the QKV projection (M = 1024 ... 65536)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the single-projection workloads (tiny, QKV M=9437, adapter switching at S=37728)")
     ap.add_argument("--unfused-mlp", action="store_true",
                     help="run gate/up and down as two plain projections (amax pass over h) instead of the "
                          "MLP's producer fusion")
@@ -259,6 +264,242 @@ class Block:
                 raise RuntimeError(f"device status {v} in projection {d['name']}")
 
 
+
+# ------------------------------------------------------- single projections
+def gemm_roofline(base_flops, lup_flops, gemm_ms, peaks):
+    """The GEMM's mixed FP4/BF16 roofline: ideal time at the burst peaks
+    (measured bf16 x the nominal FP4:BF16 ratio for the FP4 part)."""
+    peak_bf16 = peaks["bf16_tflops"]
+    peak_fp4 = peak_bf16 * FP4_OVER_BF16
+    ideal_s = base_flops / (peak_fp4 * 1e12) + lup_flops / (peak_bf16 * 1e12)
+    mixed = (base_flops + lup_flops) / ideal_s / 1e12
+    achieved = (base_flops + lup_flops) / (gemm_ms * 1e-3) / 1e12
+    return {"achieved": achieved, "peak": mixed, "unit": "TFLOP/s", "frac": achieved / mixed}
+
+
+class Projection:
+    """One projection resident on the device: x, pre_quant_scale, packed
+    weight, resident adapters, output and workspace."""
+
+    def __init__(self, x, pqs, W, adapters, silu, device, max_rank=None):
+        import torch
+
+        from nvfp4_linear_lora_gb300 import h3lin
+        self.h3lin = h3lin
+        self.M, self.K = x.shape
+        self.N = W.shape[0]
+        self.silu = silu
+        self.x = synth.to_bf16_tensor(x).to(device)
+        self.pqs = torch.from_numpy(pqs).to(device)
+        Wd = synth.to_bf16_tensor(W).to(device)
+        self.pw = h3lin.pack_weight(Wd)
+        del Wd
+        self.ads = [h3lin.Adapter(synth.to_bf16_tensor(a["A"]).to(device), synth.to_bf16_tensor(a["B"]).to(device),
+                                  a["rank"], a["alpha"]) for a in adapters]
+        self.acs = [a.c_struct() for a in self.ads]
+        self.wc = self.pw.c_struct()
+        r = max_rank if max_rank is not None else max([a["rank"] for a in adapters] + [0])
+        self.out = torch.empty((self.M, self.N // 2 if silu else self.N), dtype=torch.bfloat16, device=device)
+        self.ws = h3lin.new_workspace(h3lin.h3lin_forward_workspace_bytes(self.M, self.K, self.N, r), device)
+        self.stream = torch.cuda.current_stream().cuda_stream
+
+    def flops(self, adapter_index, strength):
+        f = 2 * self.M * self.K * self.N
+        if adapter_index is not None and strength != 0.0:
+            r = self.ads[adapter_index].rank
+            f += 2 * self.M * self.K * r + 2 * self.M * r * self.N
+        return f
+
+    def lora_up_flops(self, adapter_index, strength):
+        if adapter_index is None or strength == 0.0:
+            return 0
+        return 2 * self.M * self.ads[adapter_index].rank * self.N
+
+    def run(self, adapter_index=0, strength=1.0, gemm_event=None):
+        h = self.h3lin
+        ac = self.acs[adapter_index] if adapter_index is not None else None
+        epi = h.H3LIN_EPI_SILU_MUL if self.silu else h.H3LIN_EPI_NONE
+        if gemm_event is None:
+            st = h.h3lin_forward(self.x.data_ptr(), self.M, self.pqs.data_ptr(), self.wc, epi, ac, strength,
+                                 self.out.data_ptr(), h.H3LIN_OUT_BF16, self.ws.data_ptr(), self.ws.numel(),
+                                 self.stream)
+            if st:
+                raise h.H3linError(st, "h3lin_forward")
+            return
+        st = h.h3lin_forward_prepare(self.x.data_ptr(), self.M, self.pqs.data_ptr(), self.wc, ac, strength,
+                                     self.ws.data_ptr(), self.ws.numel(), self.stream)
+        if st:
+            raise h.H3linError(st, "h3lin_forward_prepare")
+        gemm_event[0].record()
+        st = h.h3lin_forward_gemm(self.M, self.wc, epi, ac, strength, self.out.data_ptr(), h.H3LIN_OUT_BF16,
+                                  self.ws.data_ptr(), self.ws.numel(), self.stream)
+        if st:
+            raise h.H3linError(st, "h3lin_forward_gemm")
+        gemm_event[1].record()
+
+    def check_status(self):
+        v = self.h3lin.read_status(self.ws)
+        if v != 0:
+            raise RuntimeError(f"device status {v}")
+
+
+def time_calls(proj, calls, steps, warmup):
+    """Run the call list (adapter index or None, strength) `steps` times after
+    `warmup` untimed rounds; CUDA events around the whole region and around
+    every GEMM.  Returns (ms per round, GEMM ms per round)."""
+    import torch
+    for _ in range(warmup):
+        for ai, sv in calls:
+            proj.run(ai, sv)
+    torch.cuda.synchronize()
+    proj.check_status()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+          for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(steps):
+        for j, (ai, sv) in enumerate(calls):
+            proj.run(ai, sv, ev[k][j])
+    t1.record()
+    torch.cuda.synchronize()
+    proj.check_status()
+    gemm = sum(statistics.mean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(steps))
+               for j in range(len(calls)))
+    return t0.elapsed_time(t1) / steps, gemm
+
+
+def oracle_projection_sample(x, pqs, W, adapter, silu, m_rows, n_cols, seed):
+    """The oracle on a row x output-column sample of one projection: (seconds, flops)."""
+    from oracle import linear
+    rng = np.random.default_rng(seed)
+    N, K = W.shape
+    if silu:
+        c = np.sort(rng.choice(N // 2, min(n_cols // 2, N // 2), replace=False))
+        cols = np.concatenate([c, c + N // 2])
+    else:
+        cols = np.sort(rng.choice(N, min(n_cols, N), replace=False))
+    rows = np.sort(rng.choice(x.shape[0], min(m_rows, x.shape[0]), replace=False))
+    t0 = time.perf_counter()
+    wq, ws, tsw = linear.pack_weight(W[cols])
+    ad = None
+    if adapter is not None:
+        ad = dict(adapter)
+        ad["B"] = adapter["B"][cols]
+    linear.forward(x[rows], (wq, ws, tsw), pqs, ad, 1.0, silu)
+    dt = time.perf_counter() - t0
+    r = adapter["rank"] if adapter is not None else 0
+    return dt, 2 * len(rows) * (K * len(cols) + K * r + r * len(cols))
+
+
+def projection_line(name, proj, calls, steps, warmup, peaks, host=None, what=""):
+    """One workload's JSON object: ms, TFLOP/s, the GEMM's roofline, and
+    (with host inputs) the oracle on a small sample of the same workload."""
+    ms, gemm_ms = time_calls(proj, calls, steps, warmup)
+    flops = sum(proj.flops(ai, sv) for ai, sv in calls)
+    base = 2 * proj.M * proj.K * proj.N * len(calls)
+    lup = sum(proj.lora_up_flops(ai, sv) for ai, sv in calls)
+    line = {"workload": name, "M": proj.M, "K": proj.K, "N": proj.N, "calls_per_step": len(calls),
+            "ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+            "frac_of_fp4_peak": flops / (ms * 1e-3) / 1e12 / (peaks["bf16_tflops"] * FP4_OVER_BF16),
+            "gemm_ms_per_step": gemm_ms, "prepare_ms_per_step": ms - gemm_ms,
+            "roofline": dict(kernel="k_fp4gemm", bound="tensor", **gemm_roofline(base, lup, gemm_ms, peaks)),
+            "what": what}
+    if host is not None:
+        x, pqs, W, adapter, silu = host
+        t, f = oracle_projection_sample(x, pqs, W, adapter, silu, 64, 512, seed=proj.M)
+        line["cpu_baseline"] = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cpu_info(), "kind": "oracle",
+                                "sample": f"64 rows x 512 output columns, {t:.2f} s"}
+    return line
+
+
+def _tiny_inputs():
+    t = configs.TINY
+    p = synth.projection(t["seed"], t["M"], t["K"], t["N"], t["rank"])
+    return p["x"], p["pqs"], p["W"], [p["adapter"]]
+
+
+def _qkv_inputs():
+    q = configs.QKV
+    p = synth.projection(q["seed"], q["M"], q["K"], q["N"], q["rank"], outlier_frac=q["outlier_frac"])
+    return p["x"], p["pqs"], p["W"], [p["adapter"]]
+
+
+def _switch_inputs():
+    # two resident adapters (rank 384 and 128, their own seeds) on the QKV shape at S = 37728
+    rng = np.random.default_rng(configs.SWITCH_SEED)
+    K, N = configs.HIDDEN, 3 * configs.HIDDEN
+    x = synth.activation(rng, configs.SWITCH_S, K, "normal", 0.01)
+    s = synth.pre_quant_scale(rng, K)
+    W = synth.weight(rng, N, K)
+    ads = [synth.adapter(np.random.default_rng(sd), N, K, r) for sd, r in zip(configs.SWITCH_ADAPTER_SEEDS, (384, 128))]
+    return x, s, W, ads
+
+
+def _sweep_inputs(M, seed):
+    K, N, r = configs.HIDDEN, 3 * configs.HIDDEN, 384
+    rng = np.random.default_rng(seed)
+    x = synth.activation(rng, M, K, "student_t3", 0.01)
+    s = synth.pre_quant_scale(rng, K)
+    W = synth.weight(rng, N, K)
+    return x, s, W, [synth.adapter(rng, N, K, r)]
+
+
+def start_workload_inputs(a, pool):
+    """Host inputs of the single-projection workloads, drawn on worker threads
+    (each from its own seeded generator) while the block is set up and timed."""
+    futs = {}
+    if not a.no_configs:
+        futs["tiny"] = pool.submit(_tiny_inputs)
+        futs["qkv_9437"] = pool.submit(_qkv_inputs)
+        futs["switch_S37728"] = pool.submit(_switch_inputs)
+    if not a.no_sweep:
+        for M, seed in zip(configs.SWEEP_M, configs.SWEEP_SEEDS):
+            futs[f"sweep_M{M}"] = pool.submit(_sweep_inputs, M, seed)
+    return futs
+
+
+def workload_lines(a, device, peaks, futs):
+    """Throughput on the single-projection workloads (the tiny projection, the
+    QKV projection at M = 9437, adapter switching at S = 37728) and the
+    sequence-length sweep of the QKV projection."""
+    import torch
+    steps, warmup = max(5, a.steps // 10), 3
+    out = {}
+    if not a.no_configs:
+        x, s, W, ads = futs.pop("tiny").result()
+        pr = Projection(x, s, W, ads, False, device)
+        out["tiny"] = projection_line("tiny", pr, [(0, 1.0)], steps, warmup, peaks, host=(x, s, W, ads[0], False),
+                                      what="M=200 K=256 N=384 rank 16 (launch-bound: three kernels for 0.04 GFLOP)")
+        x, s, W, ads = futs.pop("qkv_9437").result()
+        pr = Projection(x, s, W, ads, False, device)
+        out["qkv_9437"] = projection_line("qkv_9437", pr, [(0, 1.0)], steps, warmup, peaks,
+                                          host=(x, s, W, ads[0], False),
+                                          what="fused QKV 5120->15360 rank 384, M=9437 (ragged), 1% outlier channels")
+        del pr
+        x, s, W, ads = futs.pop("switch_S37728").result()
+        pr = Projection(x, s, W, ads, False, device)
+        calls = [(0, 1.0), (1, 0.5), (None, 1.0), (0, 0.0), (1, 1.0), (0, 0.5)]
+        out["switch_S37728"] = projection_line(
+            "switch_S37728", pr, calls, steps, warmup, peaks,
+            what="QKV shape at S=37728, per call: adapter a (rank 384) s=1, b (rank 128) s=0.5, NULL, a s=0, "
+                 "b s=1, a s=0.5; FLOPs count the LoRA only where it runs (strength 0 and NULL take the base path)")
+        del pr
+    sweep = None
+    if not a.no_sweep:
+        sweep = []
+        for M in configs.SWEEP_M:
+            x, s, W, ads = futs.pop(f"sweep_M{M}").result()
+            pr = Projection(x, s, W, ads, False, device)
+            line = projection_line(f"sweep_M{M}", pr, [(0, 1.0)], steps, warmup, peaks,
+                                   host=(x, s, W, ads[0], False),
+                                   what="QKV 5120->15360 rank 384, Student-t(3) activations with 1% outlier channels")
+            tiles = ((M + 255) // 256) * (pr.N // 256)
+            line["gemm_tiles"] = tiles
+            line["gemm_tile_waves"] = tiles / (torch.cuda.get_device_properties(device).multi_processor_count // 2)
+            sweep.append(line)
+            del pr
+    return out, sweep
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -414,6 +655,9 @@ def native_arm(a, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     S = a.S
+    import concurrent.futures as cf
+    pool = cf.ThreadPoolExecutor(max_workers=4)
+    futs = start_workload_inputs(a, pool) if rank == 0 else {}
     host = make_block_inputs(S)
     blk = Block(host, S, device, fused_mlp=not a.unfused_mlp)
     peaks, peak_kind = load_peaks()
@@ -651,29 +895,33 @@ def native_arm(a, rank, world, local_rank):
                           "compute (double-buffered device inputs and outputs)"}
 
     if rank != 0:
+        pool.shutdown(wait=False)
         return 0
 
-    # roofline of the dominant kernel (the FP4 GEMM with LoRA-up), live event timing
+    # the single-projection workloads and the sweep (their inputs were drawn
+    # on worker threads meanwhile; all drawn before the CPU baseline is timed)
+    workloads, sweep = workload_lines(a, device, peaks, futs)
+    pool.shutdown(wait=True)
+
+    # roofline of the dominant kernel (the FP4 GEMM with LoRA-up), live event
+    # timing; peaks are the burst figures (the timed region is about a second,
+    # not a seconds-long power-capped loop)
     gemm_total_ms = sum(gemm_ms)
-    gemm_fp4 = base
-    gemm_bf16 = lup
-    peak_bf16 = peaks["bf16_tflops_sustained"]
+    peak_bf16 = peaks["bf16_tflops"]
     peak_fp4 = peak_bf16 * FP4_OVER_BF16
-    ideal_s = gemm_fp4 / (peak_fp4 * 1e12) + gemm_bf16 / (peak_bf16 * 1e12)
-    mixed_peak = (gemm_fp4 + gemm_bf16) / ideal_s / 1e12
-    achieved = (gemm_fp4 + gemm_bf16) / (gemm_total_ms * 1e-3) / 1e12
+    rf = gemm_roofline(base, lup, gemm_total_ms, peaks)
     alg = gemm_algorithmic_bytes(S)
     traffic = None
     if GEMM_TRAFFIC["sources_sha256"] == gemm_sources_sha256() and GEMM_TRAFFIC["S"] == S:
         traffic = sum(GEMM_TRAFFIC["bytes_per_launch"].values())
-    roofline = {"kernel": "k_fp4gemm", "bound": "tensor", "achieved": achieved, "peak": mixed_peak,
-                "unit": "TFLOP/s", "frac": achieved / mixed_peak, "traffic": traffic,
+    roofline = {"kernel": "k_fp4gemm", "bound": "tensor", **rf, "traffic": traffic,
                 "traffic_scope": "DRAM bytes of the block's four GEMM launches (read + write), as achieved is "
                                  "the FLOPs of those four launches over their summed time",
                 "algorithmic_bytes": sum(alg.values()),
                 "traffic_per_launch": dict(GEMM_TRAFFIC["bytes_per_launch"]) if traffic else None,
-                "peak_basis": f"{peak_kind} sustained bf16 {peak_bf16:.1f} TF/s x {FP4_OVER_BF16:g} for the FP4 "
-                              f"part, x 1 for the BF16 LoRA-up part, time-weighted over this kernel's FLOP mix",
+                "peak_basis": f"{peak_kind} burst bf16 {peak_bf16:.1f} TF/s x {FP4_OVER_BF16:g} for the FP4 part "
+                              f"(FP4 {peak_fp4:.0f} TF/s), x 1 for the BF16 LoRA-up part, time-weighted over this "
+                              f"kernel's FLOP mix",
                 "gemm_ms_per_projection": dict(zip([d["name"] for d in blk.proj], gemm_ms))}
 
     cpu = None
@@ -691,15 +939,15 @@ def native_arm(a, rank, world, local_rank):
     if merged_line is not None:
         mms = merged_line["ms_per_block"]
         lora_ms = ms - mms
-        lora_tf = (ldown + lup) / (lora_ms * 1e-3) / 1e12 if lora_ms > 0 else None
         split = {"base_only": {"ms_per_block": mms, "tflops": world * base / (mms * 1e-3) / 1e12,
                                "frac_of_fp4_peak": base / (mms * 1e-3) / 1e12 / peak_fp4},
-                 "lora_part": {"ms_per_block": lora_ms, "tflops": None if lora_tf is None else world * lora_tf,
-                               "frac_of_bf16_peak": None if lora_tf is None else lora_tf / peak_bf16},
+                 "lora_part": {"ms_per_block": lora_ms,
+                               "marginal_tflops": None if lora_ms <= 0 else (ldown + lup) / (lora_ms * 1e-3) / 1e12},
                  "how": "base only = the block with every adapter merged into its weight (merged_lora: the same "
                         "base work, no LoRA branch); LoRA part = the dynamic block's extra time over it, for the "
-                        "A(x) and B(u) FLOPs (a marginal cost: A(x) runs inside the HBM-bound amax pass, where "
-                        "it partly hides, so this fraction can exceed 1); peaks as in frac_of_fp4_peak and roofline"}
+                        "A(x) and B(u) FLOPs: a marginal time (A(x) runs inside the HBM-bound amax pass, where it "
+                        "partly hides), not a kernel's fraction of a peak"}
+
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -710,10 +958,16 @@ def native_arm(a, rank, world, local_rank):
                                    else "unfused (separate amax pass over h)",
                        "l2": f"inputs larger than L2 (each activation >= {S * configs.HIDDEN * 2 / 1e6:.0f} MB), no flush"},
             "ms_per_block": ms, "frac_of_fp4_peak": value / world / peak_fp4,
+            "frac_of_fp4_nominal": value / world / FP4_NOMINAL_TFLOPS,
+            "fp4_peak_basis": f"frac_of_fp4_peak: {peak_kind} burst bf16 {peak_bf16:.1f} TF/s x {FP4_OVER_BF16:g} = "
+                              f"{peak_fp4:.0f} TF/s; frac_of_fp4_nominal: datasheet dense FP4 {FP4_NOMINAL_TFLOPS:.0f} "
+                              f"TF/s; SM clock median in the timed region: "
+                              f"{clocks.get('sm_mhz') if clocks else None} MHz",
             "flops_per_block": {"total": total, "base_fp4": base, "lora_down": ldown, "lora_up": lup},
             "kernel_ms": {"gemm": gemm_total_ms, "prepare": ms - gemm_total_ms},
             "roofline": roofline, "peak_split": split, "cpu_baseline": cpu, "e2e": e2e, "merged_lora": merged_line,
             "qk_norm_rope": rope_line, "modulation": mod_line,
+            "configs": workloads, "sweep": sweep,
             "gpu_launches": blk.launches_per_step() * a.steps, "clocks": clocks,
             "peaks": {"kind": peak_kind, **peaks}}
     print(json.dumps(line), flush=True)

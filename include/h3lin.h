@@ -108,6 +108,20 @@ size_t h3lin_quant_workspace_bytes(void);
  * LoRA intermediate A(x), the scaled copy of B and the quantiser header. */
 size_t h3lin_forward_workspace_bytes(int64_t M, int64_t K, int64_t N, int32_t max_rank);
 
+/* Byte offsets of the regions inside a forward workspace for (M, K, N, rank),
+ * for inspection (the kernels' intermediates are not part of the output):
+ *   offsets[0]  quantised activation codes, u8 [M, K/2]
+ *   offsets[1]  its E4M3 scales, native layout (h3lin_scales_bytes(M, K) bytes)
+ *   offsets[2]  u = A(x), bf16 [M, rank] row-major
+ *   offsets[3]  B' = bf16(B * strength * (alpha / rank) / (ts_x * ts_w)), [N, rank]
+ *   offsets[4]  ts_x, the activation's tensor scale (fp32)
+ *   offsets[5]  the device status word (u32)
+ * When ts_x * ts_w is so small that B' would leave the bf16 range, a power
+ * of two 2^E moves from B' to u (u holds A(x) * 2^E); the product u B', which
+ * is all the GEMM uses, is the same.  Returns H3LIN_E_SHAPE for shapes
+ * h3lin_forward_workspace_bytes rejects, H3LIN_E_INVALID for a null array. */
+h3lin_status h3lin_forward_workspace_regions(int64_t M, int64_t K, int64_t N, int32_t rank, size_t* offsets);
+
 /* Zero the status word and header of a workspace (enqueued on `stream`).
  * Call once after allocating a workspace, and after reading an error. */
 h3lin_status h3lin_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
@@ -116,8 +130,9 @@ h3lin_status h3lin_workspace_init(void* workspace, size_t workspace_bytes, cudaS
 /* Dynamic NVFP4 quantisation of an activation (Ultra Fast README, "Kernel
  * path", item 1) with the checkpoint's per-input-channel pre_quant_scale
  * (TURBO.md, "Implementation"):  v = x * s in FP32, ts = amax|v| / 2688,
- * per-16 E4M3 scale = RNE_sat(blockamax / (6 ts)), codes = RNE_sat(v / (scale ts))
- * (the division taken as v * (1 / (scale * ts))).
+ * per-16 E4M3 scale = RNE_sat(blockamax / (6 ts)), codes = RNE_sat(v / (scale ts)),
+ * every step in float32 with round to nearest even (the code from the IEEE
+ * quotient; a block whose scale * ts is 0 gets all-zero codes).
  *   x                device bf16 [M, K] row-major
  *   pre_quant_scale  device fp32 [K], or NULL for all ones
  *   codes            device u8 [M, K/2]                (output)

@@ -163,7 +163,7 @@ h3lin_status quantize_impl(const void* x, int64_t M, int64_t K, const float* pqs
   const RowPlan plan = plan_rows(M, K, d.sm_count);
   if (launch_amax(x, int(M), int(K), pqs, partials, plan, nullptr, stream) != cudaSuccess) return H3LIN_E_CUDA;
   if (launch_quant(x, int(M), int(K), pqs, partials, plan.blocks, nullptr, codes, scales, ts, plan, nullptr,
-                   nullptr, 0, 0.0f, nullptr, d.sm_count, stream) != cudaSuccess)
+                   nullptr, 0, 0.0f, nullptr, nullptr, 0, d.sm_count, stream) != cudaSuccess)
     return H3LIN_E_CUDA;
   return H3LIN_OK;
 }
@@ -280,7 +280,8 @@ h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
   if (launch_quant(c.x, int(c.M), int(c.K), c.pqs, partials, nparts, c.produced ? produced_count : nullptr, xq, xs,
                    ts_x, plan,
                    c.lora ? c.adapter->B : nullptr, c.lora ? bp : nullptr, c.lora ? c.N * c.rank : 0, lora_k,
-                   c.w->tensor_scale, c.dev.sm_count, stream) != cudaSuccess)
+                   c.w->tensor_scale, c.lora ? u : nullptr, c.lora ? c.M * c.rank : 0, c.dev.sm_count,
+                   stream) != cudaSuccess)
     return H3LIN_E_CUDA;
   return H3LIN_OK;
 }
@@ -379,6 +380,19 @@ size_t h3lin_quant_workspace_bytes(void) { return kHeaderBytes; }
 size_t h3lin_forward_workspace_bytes(int64_t M, int64_t K, int64_t N, int32_t max_rank) {
   if (M < 0 || K < 64 || K % 64 != 0 || N < 1 || max_rank < 0) return 0;
   return forward_layout(M, K, N, max_rank).total;
+}
+
+h3lin_status h3lin_forward_workspace_regions(int64_t M, int64_t K, int64_t N, int32_t rank, size_t* offsets) {
+  if (!offsets) return H3LIN_E_INVALID;
+  if (M < 0 || K < 64 || K % 64 != 0 || N < 1 || rank < 0) return H3LIN_E_SHAPE;
+  const ForwardLayout L = forward_layout(M, K, N, rank);
+  offsets[0] = L.codes;
+  offsets[1] = L.scales;
+  offsets[2] = L.u;
+  offsets[3] = L.b;
+  offsets[4] = kTsOffset;
+  offsets[5] = kStatusOffset;
+  return H3LIN_OK;
 }
 
 h3lin_status h3lin_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {

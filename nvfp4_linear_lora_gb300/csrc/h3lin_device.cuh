@@ -271,6 +271,44 @@ __device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1,
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// ------------------------------------------- LoRA operand and epilogue scales
+// The GEMM accumulates the base products and u.B' in one FP32 tile and
+// multiplies the sum by ts_x * ts_w in its epilogue, so B' = B * c with
+// c = lora_k / (ts_x * ts_w).  For tiny tensor scales c leaves the bf16 range
+// although the LoRA product itself is representable; then a power of two 2^E
+// moves from B' to u (u' = u * 2^E exactly, B' = B * c * 2^-E: the same
+// product, both operands in range).  E = 0, and c = fl(lora_k / fl(ts_x ts_w))
+// bit for bit, whenever those values are normal floats with c below 2^64.
+struct LoraScale {
+  float c;       // multiplier of B
+  float u_mul;   // 2^E, multiplier of u (1 normally)
+};
+__device__ __forceinline__ LoraScale lora_scale(float lora_k, float ts_x, float ts_w) {
+  const int ex = ilogbf(ts_x), ew = ilogbf(ts_w);
+  const float m = __fmul_rn(scalbnf(ts_x, -ex), scalbnf(ts_w, -ew));   // in [1, 4)
+  const float cm = __fdiv_rn(lora_k, m);
+  const int e = -(ex + ew);                                            // c = cm * 2^e
+  int E = 0;
+  if (cm != 0.0f) E = min(max(e + ilogbf(cm) - 64, 0), 126);
+  return LoraScale{scalbnf(cm, e - E), scalbnf(1.0f, E)};
+}
+
+// The epilogue's y = ts_x * ts_w * acc as fl(fl(acc * a) * b): (a, b) =
+// (fl(ts_x ts_w), 1) while that product is at least 2^-100; below, a is the
+// product scaled up by 2^k (exactly) and b = 2^-k, so outputs in the normal
+// float range keep full precision however small the two tensor scales are.
+struct EpiScale {
+  float a, b;
+};
+__device__ __forceinline__ EpiScale epi_scale(float ts_x, float ts_w) {
+  const float p = __fmul_rn(ts_x, ts_w);
+  if (p >= 0x1p-100f) return EpiScale{p, 1.0f};
+  const int ex = ilogbf(ts_x), ew = ilogbf(ts_w);
+  const float m = __fmul_rn(scalbnf(ts_x, -ex), scalbnf(ts_w, -ew));   // in [1, 4); product = m * 2^(ex + ew)
+  const int k = min(-(ex + ew), 126);
+  return EpiScale{scalbnf(m, ex + ew + k), scalbnf(1.0f, -k)};
+}
+
 // Byte offset of the scale of (row, 16-block j) in the native scale layout.
 __host__ __device__ __forceinline__ int64_t sf_offset(int64_t row, int64_t j, int64_t K) {
   const int64_t atom = (row >> 7) * (K >> 6) + (j >> 2);

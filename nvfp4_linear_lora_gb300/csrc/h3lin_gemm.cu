@@ -3,7 +3,8 @@
 //
 //   acc[m, n]  = sum_k E2M1(xq) E4M3(sx) * E2M1(wq) E4M3(sw)   (FP4 tensor cores)
 //   acc[m, n] += sum_j u[m, j] * B'[n, j]                        (BF16 tensor cores)
-//   y          = ts_x * ts_w * acc                               (B' carries 1/(ts_x ts_w))
+//   y          = ts_x * ts_w * acc                               (B' carries 1/(ts_x ts_w);
+//                                                                  epi_scale for tiny scales)
 //   out        = y, or silu(y_gate) * y_up                       (bf16 or fp32, rows >= M masked)
 //
 // This is `NVFP4_base(x) + strength * (alpha/rank) * B(A(x))` of TURBO.md
@@ -240,7 +241,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;     // which half of the tile's columns
-    const float scale = __fmul_rn(*ts_x, *ts_w);
+    const EpiScale es = epi_scale(*ts_x, *ts_w);
+    const float scale = es.a, post = es.b;
+    const bool two = post != 1.0f;   // tiny tensor scales only
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       int tm, tn;
@@ -276,8 +279,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
               float hv[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const float g = __fmul_rn(scale, __uint_as_float(v[i][8 * w + e]));
-                const float u = __fmul_rn(scale, __uint_as_float(v[2 + i][8 * w + e]));
+                float g = __fmul_rn(scale, __uint_as_float(v[i][8 * w + e]));
+                float u = __fmul_rn(scale, __uint_as_float(v[2 + i][8 * w + e]));
+                if (two) {
+                  g = __fmul_rn(g, post);
+                  u = __fmul_rn(u, post);
+                }
                 hv[e] = __fmul_rn(silu(g), u);
               }
               store8<F32OUT>(out_row, col0 + 32 * i + 8 * w, hv);
@@ -291,7 +298,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
             for (int w = 0; w < 4; ++w) {
               float hv[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) hv[e] = __fmul_rn(scale, __uint_as_float(v[i][8 * w + e]));
+              for (int e = 0; e < 8; ++e) {
+                hv[e] = __fmul_rn(scale, __uint_as_float(v[i][8 * w + e]));
+                if (two) hv[e] = __fmul_rn(hv[e], post);
+              }
               store8<F32OUT>(out_row, col0 + 32 * i + 8 * w, hv);
             }
           }
@@ -366,19 +376,60 @@ struct PairCfg {
 
 // silu(g) * u with g = scale * acc_gate, u = scale * acc_up (fast exp and divide;
 // for very negative g the quotient underflows to 0, the limit of g / (1 + e^-g)).
-__device__ __forceinline__ float silu_mul_fast(float scale, uint32_t acc_g, uint32_t acc_u) {
-  const float g = __fmul_rn(scale, __uint_as_float(acc_g));
-  const float u = __fmul_rn(scale, __uint_as_float(acc_u));
+// TWO: each of g and u is then multiplied by post (epi_scale's second factor).
+template <bool TWO>
+__device__ __forceinline__ float silu_mul_fast(float scale, float post, uint32_t acc_g, uint32_t acc_u) {
+  float g = __fmul_rn(scale, __uint_as_float(acc_g));
+  float u = __fmul_rn(scale, __uint_as_float(acc_u));
+  if (TWO) {
+    g = __fmul_rn(g, post);
+    u = __fmul_rn(u, post);
+  }
   return __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
 }
 // The same for two adjacent columns, the multiplies paired (identical results;
 // the epilogue's instruction count shows up in the MMA issue rate).
-__device__ __forceinline__ uint32_t silu_mul2_bf16(float scale, uint32_t g0, uint32_t g1, uint32_t u0, uint32_t u1) {
+template <bool TWO>
+__device__ __forceinline__ uint32_t silu_mul2_bf16(float scale, float post, uint32_t g0, uint32_t g1, uint32_t u0,
+                                                   uint32_t u1) {
   float ga, gb, ua, ub, oa, ob;
   fmul2_rn(__uint_as_float(g0), __uint_as_float(g1), scale, scale, ga, gb);
   fmul2_rn(__uint_as_float(u0), __uint_as_float(u1), scale, scale, ua, ub);
+  if (TWO) {
+    fmul2_rn(ga, gb, post, post, ga, gb);
+    fmul2_rn(ua, ub, post, post, ua, ub);
+  }
   fmul2_rn(__fdividef(ga, 1.0f + __expf(-ga)), __fdividef(gb, 1.0f + __expf(-gb)), ua, ub, oa, ob);
   return pack_bf16x2(oa, ob);
+}
+
+// One staging row's worth (16 words) of a pair-epilogue warp's output from its
+// accumulator columns a (0..31) and b (32..63, or the up half for SiLU*up).
+template <bool SILU, bool F32OUT, bool TWO>
+__device__ __forceinline__ void epi_convert(float scale, float post, const uint32_t (&a)[32], const uint32_t (&b)[32],
+                                            int rd, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    if (F32OUT) {
+      const int c = rd * 16 + k;   // output column of this warp
+      if (SILU) {
+        w[k] = __float_as_uint(silu_mul_fast<TWO>(scale, post, a[c], b[c]));
+      } else {
+        float y = __fmul_rn(scale, __uint_as_float(c < 32 ? a[c] : b[c - 32]));
+        if (TWO) y = __fmul_rn(y, post);
+        w[k] = __float_as_uint(y);
+      }
+    } else if (SILU) {
+      w[k] = silu_mul2_bf16<TWO>(scale, post, a[2 * k], a[2 * k + 1], b[2 * k], b[2 * k + 1]);
+    } else {
+      const int c = rd * 32 + 2 * k;
+      const uint32_t lo = c < 32 ? a[c] : b[c - 32], hi = c < 32 ? a[c + 1] : b[c - 31];
+      float ylo, yhi;
+      fmul2_rn(__uint_as_float(lo), __uint_as_float(hi), scale, scale, ylo, yhi);
+      if (TWO) fmul2_rn(ylo, yhi, post, post, ylo, yhi);
+      w[k] = pack_bf16x2(ylo, yhi);
+    }
+  }
 }
 
 // The warp's staging block (32 rows x 64 bytes, 16-byte chunks placed as the
@@ -431,6 +482,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_cp + kPairCpWarps);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* amax_red = reinterpret_cast<float*>(abort_flag + 1);   // one per epilogue warp (AMAX)
+  float* epi_post = amax_red + C::kEpiWarps;                     // epi_scale's second factor (1 normally)
 
   const int warp = warp_id(), lane = lane_id();
   const uint32_t crank = cluster_ctarank();
@@ -446,6 +498,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     mbar_init(drain_bar, 1);
     for (int w = 0; w < kPairCpWarps; ++w) mbar_init(&drain_cp[w], 1);
     *abort_flag = 0;
+    *epi_post = epi_scale(*ts_x, *ts_w).b;
     fence_mbar_init();
     tma_prefetch_desc(&tm_xq);
     tma_prefetch_desc(&tm_wq);
@@ -625,7 +678,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     const int e = warp - kPairEpiWarp0;
     const int c4 = e >> 2;                   // which quarter of the tile's columns
     uint8_t* scratch = epi_scratch + e * C::kEpiScratch;
-    const float scale = __fmul_rn(*ts_x, *ts_w);
+    const float scale = epi_scale(*ts_x, *ts_w).a;
     const uint32_t leader_tmem_empty = cluster_addr(tmem_empty, 0);
     constexpr int kEsize = F32OUT ? 4 : 2;
     constexpr int kRoundCols = 64 / kEsize;          // output columns per 64-byte staging row
@@ -652,22 +705,11 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
 #pragma unroll
       for (int rd = 0; rd < kRounds; ++rd) {
         uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          if (F32OUT) {
-            const int c = rd * 16 + k;   // output column of this warp
-            w[k] = SILU ? __float_as_uint(silu_mul_fast(scale, a[c], b[c]))
-                        : __float_as_uint(__fmul_rn(scale, __uint_as_float(c < 32 ? a[c] : b[c - 32])));
-          } else if (SILU) {
-            w[k] = silu_mul2_bf16(scale, a[2 * k], a[2 * k + 1], b[2 * k], b[2 * k + 1]);
-          } else {
-            const int c = rd * 32 + 2 * k;
-            const uint32_t lo = c < 32 ? a[c] : b[c - 32], hi = c < 32 ? a[c + 1] : b[c - 31];
-            float ylo, yhi;
-            fmul2_rn(__uint_as_float(lo), __uint_as_float(hi), scale, scale, ylo, yhi);
-            w[k] = pack_bf16x2(ylo, yhi);
-          }
-        }
+        const float post = *epi_post;   // != 1 for tiny tensor scales only
+        if (post != 1.0f)
+          epi_convert<SILU, F32OUT, true>(scale, post, a, b, rd, w);
+        else
+          epi_convert<SILU, F32OUT, false>(scale, 1.0f, a, b, rd, w);
         if (AMAX && row0 + lane < M) {
           // per element: |fl(h * s)| with h the stored bf16 value (the lanes'
           // loads of s are broadcasts: all lanes read the same 32 columns)

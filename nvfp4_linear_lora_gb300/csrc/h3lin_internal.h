@@ -39,9 +39,10 @@ cudaError_t launch_amax(const void* x, int M, int K, const float* pqs, float* pa
 // of taking nparts (partials left by a producer GEMM).
 cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
                          const int* nparts_dev, void* codes, void* scales, float* ts_out, const RowPlan& p,
-                         // optional: B' = bf16(B * lora_k / (ts * ts_w)), elems % 8 == 0
+                         // optional: B' = bf16(B * lora_k / (ts * ts_w)), elems % 8 == 0; u (bf16,
+                         // written by the amax pass) takes a power of two from B' for tiny tensor scales
                          const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
-                         int sm_count, cudaStream_t st);
+                         void* u, int64_t u_elems, int sm_count, cudaStream_t st);
 // amax pass fused with u = A(x) (bf16 [M, rank]); returns grid size in *nparts.
 cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
                              int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,

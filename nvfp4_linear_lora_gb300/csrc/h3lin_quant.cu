@@ -9,15 +9,16 @@
 //   k_quant      reduces the partials to the tensor scale, quantises x * s to
 //                E2M1 codes + E4M3 block scales (bit-exact rules below), and
 //                optionally writes B' = B * strength * (alpha/rank) / (ts_x ts_w)
-//                so that the GEMM can accumulate B'(u) into the FP4 tile.
+//                so that the GEMM can accumulate B'(u) into the FP4 tile
+//                (for tiny tensor scales a power of two moves from B' to u).
 //   k_amax_lora<QUANT>  when a producer GEMM's epilogue already reduced the
 //                amax of x (the gate/up output feeding down): the TMA-staged
 //                pass quantises x and computes u = A(x) in one read of x.
 //
 // Quantisation rules (float32, round to nearest even at every step):
 //   v = x * s;  ts = amax / 2688 (0 -> 1);  per 16 elements:
-//   sb = E4M3_sat(blockamax / (6 ts));  d = E4M3(sb) * ts;  inv = 1 / d;
-//   code = E2M1_sat(v * inv) with the sign of v kept;  inv not finite -> 0.
+//   sb = E4M3_sat(blockamax / (6 ts));  d = E4M3(sb) * ts;
+//   code = E2M1_sat(v / d) with the sign of v kept;  d == 0 -> all codes 0.
 #include "h3lin_device.cuh"
 
 namespace h3lin {
@@ -118,16 +119,15 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict_
 // ---------------------------------------------------------------- k_quant
 // Thread t owns 16-element block b = t % (K/16) of rows r0, r0 + R, ... with
 // r0 = t / (K/16): its 16 per-channel scales stay in registers, the block
-// scale is computed once per block, and the four threads of a 64-column group
-// (never split across rows, K % 64 == 0) assemble the 32-bit scale word.
+// scale is computed once per block, and each thread stores its own scale byte.
 struct QuantCtx {
   float ts, six_ts;
   float rcp_six_ts;       // fl(1 / six_ts)
-  const float* inv_tab;   // optional: 1 / (E4M3(sb) * ts) for every scale byte sb (shared memory)
+  const float2* yt;       // bracket of 1 / d for every scale byte (shared memory, bracket_entry)
 };
-__device__ __forceinline__ QuantCtx make_quant_ctx(float ts, const float* inv_tab) {
+__device__ __forceinline__ QuantCtx make_quant_ctx(float ts, const float2* yt) {
   const float six_ts = __fmul_rn(6.0f, ts);
-  return QuantCtx{ts, six_ts, __frcp_rn(six_ts), inv_tab};
+  return QuantCtx{ts, six_ts, __frcp_rn(six_ts), yt};
 }
 
 // sb = E4M3_sat(fl(bm / (6 ts))), mostly without the division: p = fl(bm *
@@ -143,10 +143,63 @@ __device__ __forceinline__ uint32_t block_scale_byte(float bm, const QuantCtx& q
   return e4m3_rn_satfinite(p);
 }
 
-// inv_tab[sb] = 1 / fl(E4M3(sb) * ts), the same two roundings quant_block takes
-// per block, tabulated once per CTA for the 256 scale bytes.
-__device__ __forceinline__ float block_inv(float ts, uint32_t sb) {
-  return __frcp_rn(__fmul_rn(e4m3_to_float(sb), ts));
+// Element codes are E2M1(fl(v / d)), the IEEE quotient rounded once.  The
+// quotient is not taken per element: with y = fl(1 / d), the products
+// q_lo = fl(v fl(y (1 - 2^-21))) and q_hi = fl(v fl(y (1 + 2^-21))) lie
+// strictly on either side of fl(v / d) (each is at least 5 * 2^-24 away from
+// v / d in relative terms, the rounded quotient at most 2^-24, while all
+// values are normal floats, which d > 2^-100 ensures for any value that can
+// reach an E2M1 midpoint), and the E2M1 value is monotone in its argument,
+// so where q_lo and q_hi give the same code that is the quotient's code.
+// They differ only for a quotient within about 2^-21 (relative) of an E2M1
+// rounding midpoint: there, element by element, the IEEE division decides.
+// Such quotients are frequent on bf16 data (short mantissas make exact
+// midpoints of v / d common: a few elements in 10^4), so only the differing
+// elements divide.  A block with d <= 2^-100 divides every element.
+// bracket_entry(ts, sb) = (fl(y (1 - 2^-21)), fl(y (1 + 2^-21))), tabulated
+// once per CTA for the 256 scale bytes (y = inf for d == 0).
+__device__ __forceinline__ float2 bracket_entry(float ts, uint32_t sb) {
+  const float y = __frcp_rn(__fmul_rn(e4m3_to_float(sb), ts));
+  return make_float2(__fmul_rn(y, 1.0f - 0x1p-21f), __fmul_rn(y, 1.0f + 0x1p-21f));
+}
+__device__ __forceinline__ void build_bracket_table(float2* yt, float ts) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) yt[i] = bracket_entry(ts, i);
+}
+
+// E2M1 code of fl(v / d) in bits 0-3 (the slow path).
+__device__ __forceinline__ uint32_t code_by_division(float v, float d) {
+  const float q[8] = {__fdiv_rn(v, d), 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  return e2m1x8(q) & 0xFu;
+}
+
+__device__ __forceinline__ uint2 block_codes(const float (&v)[16], float2 y, float ts, uint32_t sb) {
+  float la[8], lb[8], ha[8], hb[8];
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    fmul2_rn(v[i], v[i + 1], y.x, y.x, la[i], la[i + 1]);
+    fmul2_rn(v[8 + i], v[9 + i], y.x, y.x, lb[i], lb[i + 1]);
+    fmul2_rn(v[i], v[i + 1], y.y, y.y, ha[i], ha[i + 1]);
+    fmul2_rn(v[8 + i], v[9 + i], y.y, y.y, hb[i], hb[i + 1]);
+  }
+  uint2 c = make_uint2(e2m1x8(la), e2m1x8(lb));
+  const uint32_t dx = c.x ^ e2m1x8(ha), dy = c.y ^ e2m1x8(hb);
+  const bool bracket_ok = y.y < 0x1p100f;
+  if (bracket_ok && (dx | dy) == 0u) return c;
+  const float d = __fmul_rn(e4m3_to_float(sb), ts);
+  if (d == 0.0f) return make_uint2(0u, 0u);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int sh = 4 * (i & 7);
+    const uint32_t differ = ((i < 8 ? dx : dy) >> sh) & 0xFu;
+    if (!bracket_ok || differ != 0u) {
+      const uint32_t code = code_by_division(v[i], d) << sh;
+      if (i < 8)
+        c.x = (c.x & ~(0xFu << sh)) | code;
+      else
+        c.y = (c.y & ~(0xFu << sh)) | code;
+    }
+  }
+  return c;
 }
 
 __device__ __forceinline__ void load_scale16(const float* __restrict__ pqs, int b, float (&s)[16]) {
@@ -182,17 +235,37 @@ __device__ __forceinline__ void quant_block(const QuantCtx& q, uint2* code, uint
 #pragma unroll
   for (int i = 1; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
   const uint32_t sb = block_scale_byte(bm, q);
-  const float inv = q.inv_tab ? q.inv_tab[sb] : block_inv(q.ts, sb);
-  float qa[8], qb[8];
-#pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    fmul2_rn(v[i], v[i + 1], inv, inv, qa[i], qa[i + 1]);
-    fmul2_rn(v[8 + i], v[9 + i], inv, inv, qb[i], qb[i + 1]);
-  }
-  uint2 cw = make_uint2(0u, 0u);
-  if (isfinite(inv)) cw = make_uint2(e2m1x8(qa), e2m1x8(qb));
+  const uint2 cw = block_codes(v, q.yt[sb], q.ts, sb);
   if (code) *code = cw;
   *sf = static_cast<uint8_t>(sb);
+}
+
+// B' = bf16(B * c) over [b_chunks] 16-byte chunks, grid-strided from `first`
+// by `stride`; and, when the LoRA scale moved a power of two to u (u_mul != 1),
+// u *= u_mul in place over [u_chunks] chunks (u was written by the amax pass).
+__device__ __forceinline__ void scale_lora_operands(const LoraScale& ls, const uint4* __restrict__ b_src,
+                                                    uint4* __restrict__ b_dst, int64_t b_chunks, uint4* u,
+                                                    int64_t u_chunks, int64_t first, int64_t stride) {
+  for (int64_t i = first; i < b_chunks; i += stride) {
+    const uint4 w = __ldg(b_src + i);
+    uint4 o;
+    o.x = pack_bf16x2(__fmul_rn(bf16lo(w.x), ls.c), __fmul_rn(bf16hi(w.x), ls.c));
+    o.y = pack_bf16x2(__fmul_rn(bf16lo(w.y), ls.c), __fmul_rn(bf16hi(w.y), ls.c));
+    o.z = pack_bf16x2(__fmul_rn(bf16lo(w.z), ls.c), __fmul_rn(bf16hi(w.z), ls.c));
+    o.w = pack_bf16x2(__fmul_rn(bf16lo(w.w), ls.c), __fmul_rn(bf16hi(w.w), ls.c));
+    b_dst[i] = o;
+  }
+  if (ls.u_mul != 1.0f && u != nullptr) {
+    for (int64_t i = first; i < u_chunks; i += stride) {
+      const uint4 w = u[i];
+      uint4 o;
+      o.x = pack_bf16x2(__fmul_rn(bf16lo(w.x), ls.u_mul), __fmul_rn(bf16hi(w.x), ls.u_mul));
+      o.y = pack_bf16x2(__fmul_rn(bf16lo(w.y), ls.u_mul), __fmul_rn(bf16hi(w.y), ls.u_mul));
+      o.z = pack_bf16x2(__fmul_rn(bf16lo(w.z), ls.u_mul), __fmul_rn(bf16hi(w.z), ls.u_mul));
+      o.w = pack_bf16x2(__fmul_rn(bf16lo(w.w), ls.u_mul), __fmul_rn(bf16hi(w.w), ls.u_mul));
+      u[i] = o;
+    }
+  }
 }
 
 // Rows are visited from the last to the first: the amax pass streamed them
@@ -201,8 +274,10 @@ __global__ void __launch_bounds__(kQuantThreads, 4) k_quant(
     const uint4* __restrict__ x, int M, int Mpad, int K, const float* __restrict__ pqs,
     const float* __restrict__ partials, int nparts, const int* __restrict__ nparts_dev, uint2* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ ts_out, int rows_step, const uint4* __restrict__ b_src,
-    uint4* __restrict__ b_dst, int64_t b_chunks, float lora_k, const float* __restrict__ ts_w) {
+    uint4* __restrict__ b_dst, int64_t b_chunks, float lora_k, const float* __restrict__ ts_w, uint4* u,
+    int64_t u_chunks) {
   __shared__ float red[kQuantThreads / 32];
+  __shared__ float2 yt[256];
   float m = 0.0f;
   if (nparts_dev) nparts = min(max(*nparts_dev, 0), kMaxPartials);   // never read past the partials
   for (int i = threadIdx.x; i < nparts; i += kQuantThreads) m = fmaxf(m, partials[i]);
@@ -211,7 +286,9 @@ __global__ void __launch_bounds__(kQuantThreads, 4) k_quant(
   if (ts == 0.0f) ts = 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
   const int kb = K >> 4;
-  const QuantCtx q = make_quant_ctx(ts, nullptr);
+  build_bracket_table(yt, ts);
+  __syncthreads();
+  const QuantCtx q = make_quant_ctx(ts, yt);
 
   const int tid = blockIdx.x * kQuantThreads + threadIdx.x;
   const int b = tid % kb;
@@ -244,17 +321,9 @@ __global__ void __launch_bounds__(kQuantThreads, 4) k_quant(
     }
   }
   if (b_chunks > 0) {
-    const float cl = __fdiv_rn(lora_k, __fmul_rn(ts, *ts_w));
-    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * kQuantThreads;
-    for (int64_t i = tid; i < b_chunks; i += nthreads) {
-      const uint4 w = __ldg(b_src + i);
-      uint4 o;
-      o.x = pack_bf16x2(__fmul_rn(bf16lo(w.x), cl), __fmul_rn(bf16hi(w.x), cl));
-      o.y = pack_bf16x2(__fmul_rn(bf16lo(w.y), cl), __fmul_rn(bf16hi(w.y), cl));
-      o.z = pack_bf16x2(__fmul_rn(bf16lo(w.z), cl), __fmul_rn(bf16hi(w.z), cl));
-      o.w = pack_bf16x2(__fmul_rn(bf16lo(w.w), cl), __fmul_rn(bf16hi(w.w), cl));
-      b_dst[i] = o;
-    }
+    const LoraScale ls = lora_scale(lora_k, ts, *ts_w);
+    scale_lora_operands(ls, b_src, b_dst, b_chunks, u, u_chunks, tid,
+                        static_cast<int64_t>(gridDim.x) * kQuantThreads);
   }
 }
 
@@ -311,7 +380,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(abort_flag + 1);
-  float* inv_tab = reinterpret_cast<float*>(smem + stages * stage_bytes + 256);   // QUANT: 256 floats
+  float2* yt = reinterpret_cast<float2*>(smem + stages * stage_bytes + 256);   // QUANT: 256 brackets of 1 / d
 
   constexpr int kWorkers = lora_workers<QUANT>();
   constexpr int kThreads = lora_threads<QUANT>();
@@ -355,9 +424,12 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     ts = __fdiv_rn(m, 2688.0f);
     if (ts == 0.0f) ts = 1.0f;
     if (blockIdx.x == 0 && threadIdx.x == 0) *qo.ts_out = ts;
-    if (threadIdx.x < 256) inv_tab[threadIdx.x] = block_inv(ts, threadIdx.x);
+    build_bracket_table(yt, ts);
     __syncthreads();
   }
+  // QUANT: B' multiplier, and the power of two u carries when the tensor
+  // scales are tiny (u is written below, after ts is known)
+  const LoraScale ls = (QUANT && qo.b_chunks > 0) ? lora_scale(qo.lora_k, ts, *qo.ts_w) : LoraScale{1.0f, 1.0f};
 
   if (warp == 0) {
     if (lane == 0) {
@@ -431,7 +503,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     // QUANT: block qj of rows qr + kQuantRowStep h of each stage; its 16
     // scales are loaded one stage ahead
     const int qj = at & 3, qr = at >> 2;
-    const QuantCtx qc = make_quant_ctx(ts, inv_tab);
+    const QuantCtx qc = make_quant_ctx(ts, yt);
     constexpr int kQuantRowStep = 8 * kWorkers;       // rows covered by the workers at once
     constexpr int kQuantRows = 128 / kQuantRowStep;   // rows of a tile per thread
     // byte offset of block qj of each of this thread's rows inside a 512-byte
@@ -513,7 +585,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
         if (lane == 0) mbar_arrive(&empty[st]);
         if (++st == stages) { st = 0; ph ^= 1; }
       }
-      // epilogue: u[row, :] = bf16(acc)
+      // epilogue: u[row, :] = bf16(acc * u_mul) (u_mul = 1 but for tiny tensor scales)
       if (!mbar_wait(tmem_full, acc_ph, ab)) goto amax_done;
       tc_fence_after();
       {
@@ -527,11 +599,15 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
             uint4* dst = reinterpret_cast<uint4*>(u + static_cast<int64_t>(row) * rank + c0);
             const int nvec = (rank - c0) >= 32 ? 4 : 2;
             for (int v = 0; v < nvec; ++v) {
+              float f[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                f[i] = QUANT ? __fmul_rn(__uint_as_float(r[8 * v + i]), ls.u_mul) : __uint_as_float(r[8 * v + i]);
               uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-              o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-              o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-              o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+              o.x = pack_bf16x2(f[0], f[1]);
+              o.y = pack_bf16x2(f[2], f[3]);
+              o.z = pack_bf16x2(f[4], f[5]);
+              o.w = pack_bf16x2(f[6], f[7]);
               dst[v] = o;
             }
           }
@@ -542,19 +618,10 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
       if (lane == 0) mbar_arrive(tmem_empty);
       acc_ph ^= 1;
     }
-    if (QUANT && qo.b_chunks > 0) {
-      const float cl = __fdiv_rn(qo.lora_k, __fmul_rn(ts, *qo.ts_w));
-      const int64_t nthreads = static_cast<int64_t>(gridDim.x) * (32 * kWorkers);
-      for (int64_t i = static_cast<int64_t>(blockIdx.x) * (32 * kWorkers) + at; i < qo.b_chunks; i += nthreads) {
-        const uint4 w = __ldg(qo.b_src + i);
-        uint4 o;
-        o.x = pack_bf16x2(__fmul_rn(bf16lo(w.x), cl), __fmul_rn(bf16hi(w.x), cl));
-        o.y = pack_bf16x2(__fmul_rn(bf16lo(w.y), cl), __fmul_rn(bf16hi(w.y), cl));
-        o.z = pack_bf16x2(__fmul_rn(bf16lo(w.z), cl), __fmul_rn(bf16hi(w.z), cl));
-        o.w = pack_bf16x2(__fmul_rn(bf16lo(w.w), cl), __fmul_rn(bf16hi(w.w), cl));
-        qo.b_dst[i] = o;
-      }
-    }
+    if (QUANT && qo.b_chunks > 0)   // B' only: u already carries its power of two
+      scale_lora_operands(LoraScale{ls.c, 1.0f}, qo.b_src, qo.b_dst, qo.b_chunks, nullptr, 0,
+                          static_cast<int64_t>(blockIdx.x) * (32 * kWorkers) + at,
+                          static_cast<int64_t>(gridDim.x) * (32 * kWorkers));
   amax_done:
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -621,13 +688,13 @@ static RowPlan plan_quant(int64_t M, int64_t K, int sm_count) {
 cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
                          const int* nparts_dev, void* codes, void* scales, float* ts_out, const RowPlan& /*amax plan*/,
                          const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
-                         int sm_count, cudaStream_t st) {
+                         void* u, int64_t u_elems, int sm_count, cudaStream_t st) {
   const int Mpad = ((M + 127) / 128) * 128;
   const RowPlan p = plan_quant(M, K, sm_count);
   k_quant<<<p.blocks, kQuantThreads, 0, st>>>(
       static_cast<const uint4*>(x), M, Mpad, K, pqs, partials, nparts, nparts_dev, static_cast<uint2*>(codes),
       static_cast<uint8_t*>(scales), ts_out, p.rows_step, static_cast<const uint4*>(b_src),
-      static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w);
+      static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w, static_cast<uint4*>(u), u_elems / 8);
   return cudaGetLastError();
 }
 
@@ -638,7 +705,7 @@ static cudaError_t launch_lora_pass(const CUtensorMap& tm_x, const CUtensorMap& 
   const int stage_bytes = 16384 + rank * 128;
   constexpr int kSmemLimit = 232448;     // per CTA, one CTA per SM
   constexpr int kSmemPerSm = 233472;     // shared memory of an SM (228 KB), 1 KB of it reserved per CTA
-  const int tail = 256 + (QUANT ? 1024 : 0);   // barriers, flags, partial maxima (+ reciprocal table)
+  const int tail = 256 + (QUANT ? 2048 : 0);   // barriers, flags, partial maxima (+ bracket table)
   int tmem_cols = 32;
   while (tmem_cols < rank) tmem_cols <<= 1;
   // two CTAs per SM when their accumulators fit TMEM together and each gets a

@@ -62,6 +62,7 @@ _SIGNATURES = {
     "h3lin_quant_workspace_bytes": (_sz, []),
     "h3lin_forward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
     "h3lin_workspace_init": (_i32, [_vp, _sz, _vp]),
+    "h3lin_forward_workspace_regions": (_i32, [_i64, _i64, _i64, _i32, ctypes.POINTER(_sz)]),
     "h3lin_quantize_act": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_pack_weight": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_forward": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), _i32, ctypes.POINTER(h3lin_adapter),
@@ -129,6 +130,13 @@ def h3lin_quant_workspace_bytes():
 
 def h3lin_forward_workspace_bytes(M, K, N, max_rank):
     return lib().h3lin_forward_workspace_bytes(M, K, N, max_rank)
+
+
+def h3lin_forward_workspace_regions(M, K, N, rank):
+    """(status, [codes, scales, u, B', ts_x, status word] byte offsets)."""
+    off = (_sz * 6)()
+    st = lib().h3lin_forward_workspace_regions(M, K, N, rank, off)
+    return st, list(off)
 
 
 def h3lin_workspace_init(ws, ws_bytes, stream):

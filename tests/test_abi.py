@@ -55,6 +55,24 @@ def test_sizes():
     assert h3lin.h3lin_forward_workspace_bytes(9437, 5120, 15360, 0) < ws
 
 
+def test_workspace_regions_are_disjoint_aligned_and_inside():
+    for M, K, N, r in [(9437, 5120, 15360, 384), (1, 64, 128, 16), (200, 256, 384, 0), (37726, 13824, 5120, 128)]:
+        st, off = h3lin.h3lin_forward_workspace_regions(M, K, N, r)
+        assert st == h3lin.H3LIN_OK
+        codes, scales, u, b, ts, status = off
+        total = h3lin.h3lin_forward_workspace_bytes(M, K, N, r)
+        assert (ts, status) == (4, 0)
+        assert h3lin.h3lin_quant_workspace_bytes() <= codes
+        ends = [(codes, codes + M * K // 2), (scales, scales + h3lin.h3lin_scales_bytes(M, K)),
+                (u, u + M * r * 2), (b, b + N * r * 2)]
+        for (lo, hi), (lo2, _) in zip(ends, ends[1:]):
+            assert hi <= lo2
+        assert ends[-1][1] <= total
+        assert all(o % 1024 == 0 for o in (codes, scales, u, b))
+    assert h3lin.h3lin_forward_workspace_regions(10, 100, 128, 16)[0] == h3lin.H3LIN_E_SHAPE
+    assert h3lin.lib().h3lin_forward_workspace_regions(10, 64, 128, 16, None) == h3lin.H3LIN_E_INVALID
+
+
 A = 0x10000  # an aligned fake device address (never dereferenced on error paths)
 
 

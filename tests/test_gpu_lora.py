@@ -1,0 +1,181 @@
+"""The LoRA branch on its own, on the GPU, against the oracle.
+
+Inside the whole output the LoRA term is only a few percent of the RMS (x
+with outlier channels, B ~ 0.1 N(0, 1/r)), so the parity bar on the total
+could miss LoRA errors of several percent.  These tests isolate it:
+
+* delta = y(adapter, strength 1) - y(NULL) on the fp32 output mode, element
+  by element against the oracle's lora_delta at the parity bar, on the
+  CTA-pair kernel at full size (S = 37726 rows; QKV rank 384, the gate/up
+  linear rank 128, attention-out rank 128; the tail tile and 512 sampled
+  rows);
+* zero base weight on the pair kernel: the output is the LoRA term alone
+  (with and without SiLU*up);
+* u = A(x), the bf16 intermediate the amax pass leaves in the workspace,
+  against the oracle's t = x A^T within the bf16 rounding plus the FP32
+  accumulation bound (rank 384 takes the two-piece MMA path); the
+  quantising pass of the MLP's down projection leaves the same u bit for bit;
+* inputs of tiny magnitude (x ~ 2^-100, W ~ 2^-60 and others), where the
+  scaled copy of B would leave the bf16 range and ts_x * ts_w underflows in
+  float32: codes stay bit-exact and the output meets the bar."""
+import numpy as np
+import pytest
+
+from tests._util import assert_parity, have_gpu
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not have_gpu(), reason="needs a CUDA GPU")]
+
+torch = pytest.importorskip("torch")
+
+from nvfp4_linear_lora_gb300 import build as h3build  # noqa: E402
+from nvfp4_linear_lora_gb300 import configs, h3lin, synth  # noqa: E402
+from oracle import linear, nvfp4  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    h3build.build()
+
+
+def _dev(p, W=None):
+    W = p["W"] if W is None else W
+    a = p["adapter"]
+    return (synth.to_bf16_tensor(p["x"]).cuda(),
+            torch.from_numpy(p["pqs"]).cuda() if p["pqs"] is not None else None,
+            h3lin.pack_weight(synth.to_bf16_tensor(W).cuda()),
+            h3lin.Adapter(synth.to_bf16_tensor(a["A"]).cuda(), synth.to_bf16_tensor(a["B"]).cuda(), a["rank"],
+                          a["alpha"]))
+
+
+def _sample_rows(M, seed):
+    rng = np.random.default_rng(seed)
+    return np.array(sorted(set(range((M - 1) // 128 * 128, M)) | set(rng.choice(M, 512, replace=False).tolist())))
+
+
+def _lora_ref(p, rows=None):
+    a = p["adapter"]
+    x = p["x"] if rows is None else p["x"][rows]
+    return linear.lora_delta(x, a["A"], a["B"], a["alpha"], a["rank"], 1.0)
+
+
+def _u_region(ws, M, K, N, r):
+    st, off = h3lin.h3lin_forward_workspace_regions(M, K, N, r)
+    assert st == h3lin.H3LIN_OK
+    return ws[off[2]:off[2] + M * r * 2].view(torch.bfloat16).view(M, r)
+
+
+# ----------------------------------------------------------- delta, full size
+@pytest.mark.parametrize("name,K,N,rank", [("qkv", 5120, 15360, 384), ("gate_up_linear", 5120, 27648, 128),
+                                           ("attn_out", 5120, 5120, 128)])
+def test_lora_delta_on_the_pair_kernel_at_full_size(name, K, N, rank):
+    M = configs.BLOCK_S
+    p = synth.projection(7000 + rank + N, M, K, N, rank, outlier_frac=0.01)
+    x, s, pw, ad = _dev(p)
+    assert N % 256 == 0   # the CTA-pair GEMM
+    rows = _sample_rows(M, 17)
+    idx = torch.from_numpy(rows).cuda()
+    y1 = h3lin.forward(x, pw, s, ad, 1.0, out_dtype=torch.float32).index_select(0, idx)
+    y0 = h3lin.forward(x, pw, s, None, 1.0, out_dtype=torch.float32).index_select(0, idx)
+    torch.cuda.synchronize()
+    delta = (y1.double() - y0.double()).cpu().numpy()
+    assert_parity(delta, _lora_ref(p, rows), f"{name}: LoRA delta vs oracle")
+
+
+# ----------------------------------------------------------- zero base weight
+@pytest.mark.parametrize("rank,silu", [(384, False), (128, False), (128, True), (64, True)])
+def test_zero_base_weight_on_the_pair_kernel_is_pure_lora(rank, silu):
+    M, K, N = 2000, 1024, 2048
+    p = synth.projection(8000 + rank + silu, M, K, N, rank, outlier_frac=0.01)
+    Wz = np.zeros((N, K), dtype=np.float32)
+    x, s, pw, ad = _dev(p, Wz)
+    got = h3lin.forward(x, pw, s, ad, 1.0, silu, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    want = _lora_ref(p)
+    if silu:
+        want = linear.silu_mul(want)
+    # the base branch contributes exactly nothing
+    assert_parity(got.cpu().numpy(), want, f"pure LoRA rank {rank} silu {silu}")
+    ref = linear.forward(p["x"], linear.pack_weight(Wz), p["pqs"], p["adapter"], 1.0, silu)
+    np.testing.assert_array_equal(ref, want)
+
+
+# ------------------------------------------------------------------- u = A(x)
+def _t_bound(x, A):
+    t = x.astype(np.float64) @ A.astype(np.float64).T
+    acc = np.abs(x.astype(np.float64)) @ np.abs(A.astype(np.float64)).T
+    K = x.shape[1]
+    return t, 2.0 ** -8 * np.abs(t) + 2.0 * K * 2.0 ** -24 * acc
+
+
+@pytest.mark.parametrize("M,K,N,rank", [(2000, 5120, 15360, 384), (1537, 5120, 5120, 128), (300, 1024, 1280, 256),
+                                        (129, 512, 512, 16)])
+def test_u_is_A_of_x_within_bf16_rounding(M, K, N, rank):
+    p = synth.projection(9000 + rank, M, K, N, rank, outlier_frac=0.01)
+    x, s, pw, ad = _dev(p)
+    ws = h3lin.new_workspace(h3lin.h3lin_forward_workspace_bytes(M, K, N, rank))
+    h3lin.forward(x, pw, s, ad, 1.0, workspace=ws, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert h3lin.read_status(ws) == 0
+    u = _u_region(ws, M, K, N, rank).float().cpu().numpy()
+    t, bound = _t_bound(p["x"], p["adapter"]["A"])
+    err = np.abs(u - t)
+    assert np.all(err <= bound), f"max excess {np.max(err - bound):.3e}"
+    # and it is not trivially satisfied: u carries t to bf16 precision
+    assert np.linalg.norm(u - t) / np.linalg.norm(t) < 2.0 ** -8
+
+
+def test_quantising_pass_of_the_mlp_leaves_the_same_u():
+    # the MLP's down projection computes u = A(h) inside its quantising pass
+    # (k_amax_lora with the amax known); the plain chain computes it in the
+    # amax pass: both must leave the same bf16 u
+    M, K, Ngu, Nd, r = 700, 1024, 2048, 1024, 128
+    rng = np.random.default_rng(91)
+    x = synth.activation(rng, M, K)
+    s_gu, s_d = synth.pre_quant_scale(rng, K), synth.pre_quant_scale(rng, Ngu // 2)
+    W_gu, W_d = synth.weight(rng, Ngu, K), synth.weight(rng, Nd, Ngu // 2)
+    a_gu, a_d = synth.adapter(rng, Ngu, K, r), synth.adapter(rng, Nd, Ngu // 2, r)
+    xd = synth.to_bf16_tensor(x).cuda()
+    sg, sdn = torch.from_numpy(s_gu).cuda(), torch.from_numpy(s_d).cuda()
+    pg, pd = h3lin.pack_weight(synth.to_bf16_tensor(W_gu).cuda()), h3lin.pack_weight(synth.to_bf16_tensor(W_d).cuda())
+    ag = h3lin.Adapter(synth.to_bf16_tensor(a_gu["A"]).cuda(), synth.to_bf16_tensor(a_gu["B"]).cuda(), r, a_gu["alpha"])
+    an = h3lin.Adapter(synth.to_bf16_tensor(a_d["A"]).cuda(), synth.to_bf16_tensor(a_d["B"]).cuda(), r, a_d["alpha"])
+    ws_f = h3lin.new_workspace(h3lin.h3lin_mlp_workspace_bytes(M, K, Ngu, Nd, r))
+    h3lin.mlp_forward(xd, pg, pd, sg, sdn, ag, an, workspace=ws_f)
+    h = h3lin.forward(xd, pg, sg, ag, 1.0, True)
+    ws_c = h3lin.new_workspace(h3lin.h3lin_forward_workspace_bytes(M, Ngu // 2, Nd, r))
+    h3lin.forward(h, pd, sdn, an, 1.0, workspace=ws_c)
+    torch.cuda.synchronize()
+    uf = _u_region(ws_f, M, Ngu // 2, Nd, r)
+    uc = _u_region(ws_c, M, Ngu // 2, Nd, r)
+    assert torch.equal(uf.view(torch.int16), uc.view(torch.int16))
+
+
+# ------------------------------------------------------------ tiny magnitudes
+TINY_CASES = [
+    # x scale, W scale, N (384: single-CTA GEMM, 512: CTA pair), rank, SiLU*up
+    (2.0 ** -100, 2.0 ** -60, 384, 64, False),
+    (2.0 ** -100, 2.0 ** -60, 512, 64, False),
+    (2.0 ** -100, 2.0 ** -60, 512, 32, True),
+    (1.0, 2.0 ** -90, 512, 128, False),
+    (2.0 ** -60, 1.0, 512, 128, False),
+    (2.0 ** -120, 1.0, 256, 16, False),
+]
+
+
+@pytest.mark.parametrize("xs,wsc,N,rank,silu", TINY_CASES)
+def test_tiny_magnitudes_through_the_lora_path(xs, wsc, N, rank, silu):
+    M, K = 300, 512
+    p = synth.projection(9500 + N + rank, M, K, N, rank, outlier_frac=0.01)
+    p["x"] = synth.bf16_round(p["x"] * np.float32(xs))
+    p["W"] = synth.bf16_round(p["W"] * np.float32(wsc))
+    x, s, pw, ad = _dev(p)
+    codes, scales, ts = h3lin.quantize_act(x, s)
+    got = h3lin.forward(x, pw, s, ad, 1.0, silu, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rq, rs, rts = nvfp4.quantize(p["x"], p["pqs"])
+    assert np.float32(ts.cpu().numpy()[0]) == rts
+    assert np.array_equal(codes.cpu().numpy(), rq)
+    out = got.cpu().numpy()
+    assert np.all(np.isfinite(out))
+    ref = linear.forward(p["x"], linear.pack_weight(p["W"]), p["pqs"], p["adapter"], 1.0, silu)
+    assert_parity(out, ref, f"x*{xs:g} W*{wsc:g} N={N} r={rank} silu={silu}")

@@ -7,7 +7,8 @@ bit-identical to the unfused chain (h3lin_forward on gate/up, then on down);
 h and the down output are also checked against the oracle at the parity bar
 (h on the fp32 output mode, of which the stored bf16 h must be the exact
 rounding, as for every projection; the down output against the oracle's down
-applied to the GPU's own bf16 h)."""
+applied to the oracle's own h rounded to bf16: no oracle input comes from the
+GPU)."""
 import numpy as np
 import pytest
 
@@ -102,9 +103,9 @@ def test_mlp_matches_oracle(seed, M, K, Ngu, Nd, r_gu, r_d, pqs):
     assert torch.equal(h, h32.to(torch.bfloat16)), "stored h is not the rounding of the fp32 gate/up output"
     ref_h = linear.forward(m.x, linear.pack_weight(m.W_gu), m.s_gu, m.a_gu, 1.0, True)
     assert_parity(h32.cpu().numpy(), ref_h, "h (fp32 mode) vs oracle gate/up")
-    h_host = h.float().cpu().numpy()
-    ref_y = linear.forward(h_host, linear.pack_weight(m.W_d), m.s_d, m.a_d, 1.0, False)
-    assert_parity(y.cpu().numpy(), ref_y, "down(h) vs oracle")
+    ref_y = linear.forward(synth.bf16_round(ref_h.astype(np.float32)), linear.pack_weight(m.W_d), m.s_d, m.a_d, 1.0,
+                           False)
+    assert_parity(y.cpu().numpy(), ref_y, "down(h) vs oracle down(oracle h)")
 
 
 def test_mlp_strengths_and_disabled_down():
@@ -184,7 +185,10 @@ def test_stage_api_separate_workspaces(silu):
 def test_mlp_block_S37726_bitwise_and_sampled_parity():
     """The block's gate/up -> down at full size, in the benchmark's
     configuration: fused equals the unfused chain bit for bit, and sampled
-    rows of both outputs meet the parity bar against the oracle."""
+    rows of h meet the parity bar against the oracle.  The down projection's
+    full-size parity is checked on its own seeded input (the block test of
+    test_gpu_configs): its tensor scale spans all of h, which the oracle
+    cannot produce at this size, and oracle inputs never come from the GPU."""
     S = configs.BLOCK_S
     proj = {p[0]: p for p in configs.BLOCK_PROJECTIONS}
     _, K, Ngu, r_gu, _ = proj["gate_up"]
@@ -208,10 +212,3 @@ def test_mlp_block_S37726_bitwise_and_sampled_parity():
     amax_x = nvfp4.tensor_amax_chunked(m.x, m.s_gu)
     ref_h = linear.forward(m.x, linear.pack_weight(m.W_gu), m.s_gu, m.a_gu, 1.0, True, rows=rows, x_amax=amax_x)
     assert_parity(h32.index_select(0, idx).cpu().numpy(), ref_h, "block h")
-    del h32
-    # down on sampled rows, from the GPU's whole h (its tensor scale spans all rows)
-    h_host = hf.float().cpu().numpy()
-    amax_h = nvfp4.tensor_amax_chunked(h_host, m.s_d)
-    _, yf32 = m.fused(torch.float32)
-    ref_y = linear.forward(h_host, linear.pack_weight(m.W_d), m.s_d, m.a_d, 1.0, False, rows=rows, x_amax=amax_h)
-    assert_parity(yf32.index_select(0, idx).cpu().numpy(), ref_y, "block down")
