@@ -6,9 +6,13 @@ Max is exact and A(h) runs the same MMA sequence, so every value must be
 bit-identical to the unfused chain (h3lin_forward on gate/up, then on down);
 h and the down output are also checked against the oracle at the parity bar
 (h on the fp32 output mode, of which the stored bf16 h must be the exact
-rounding, as for every projection; the down output against the oracle's down
-applied to the oracle's own h rounded to bf16: no oracle input comes from the
-GPU)."""
+rounding, as for every projection).  The down output is not compared with
+an oracle down: the oracle cannot take the GPU's h as input, and down applied
+to the oracle's own bf16 h differs by more than the parity bar, because about
+5 % of the elements of the two h differ by one bf16 unit (the LoRA branch's
+bf16 rounding) and the NVFP4 requantisation of those inputs moves the output.
+Down's parity is checked on its own seeded inputs (test_gpu_forward,
+test_gpu_configs); the fusion, by bitwise equality with the unfused chain."""
 import numpy as np
 import pytest
 
@@ -95,7 +99,7 @@ def test_mlp_bitwise_equals_unfused_chain(seed, M, K, Ngu, Nd, r_gu, r_d, pqs):
 
 
 @pytest.mark.parametrize("seed,M,K,Ngu,Nd,r_gu,r_d,pqs", MLP_CASES[:3])
-def test_mlp_matches_oracle(seed, M, K, Ngu, Nd, r_gu, r_d, pqs):
+def test_mlp_h_matches_oracle(seed, M, K, Ngu, Nd, r_gu, r_d, pqs):
     m = Mlp(seed, M, K, Ngu, Nd, r_gu, r_d, pqs)
     h, y = m.fused(torch.float32)
     h32 = h3lin.forward(m.xd, m.pw_gu, m.sd_gu, m.ad_gu, 1.0, True, out_dtype=torch.float32)
@@ -103,9 +107,10 @@ def test_mlp_matches_oracle(seed, M, K, Ngu, Nd, r_gu, r_d, pqs):
     assert torch.equal(h, h32.to(torch.bfloat16)), "stored h is not the rounding of the fp32 gate/up output"
     ref_h = linear.forward(m.x, linear.pack_weight(m.W_gu), m.s_gu, m.a_gu, 1.0, True)
     assert_parity(h32.cpu().numpy(), ref_h, "h (fp32 mode) vs oracle gate/up")
-    ref_y = linear.forward(synth.bf16_round(ref_h.astype(np.float32)), linear.pack_weight(m.W_d), m.s_d, m.a_d, 1.0,
-                           False)
-    assert_parity(y.cpu().numpy(), ref_y, "down(h) vs oracle down(oracle h)")
+    # the fused down output is the unfused down projection of the same h
+    y_c = h3lin.forward(h, m.pw_d, m.sd_d, m.ad_d, 1.0, False, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), y_c.view(torch.int32))
 
 
 def test_mlp_strengths_and_disabled_down():
