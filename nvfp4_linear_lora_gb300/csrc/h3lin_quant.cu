@@ -166,10 +166,31 @@ __device__ __forceinline__ void build_bracket_table(float2* yt, float ts) {
   for (int i = threadIdx.x; i < 256; i += blockDim.x) yt[i] = bracket_entry(ts, i);
 }
 
-// E2M1 code of fl(v / d) in bits 0-3 (the slow path).
-__device__ __forceinline__ uint32_t code_by_division(float v, float d) {
-  const float q[8] = {__fdiv_rn(v, d), 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-  return e2m1x8(q) & 0xFu;
+// The slow path of block_codes, out of line so that the hot loop stays small:
+// element i takes the IEEE division where its two bracket codes differ (bit i
+// of `which`), or every element when `which` is all ones.
+__device__ __noinline__ uint2 block_codes_slow(const float* v, float d, uint32_t which, uint2 c) {
+  if (d == 0.0f) return make_uint2(0u, 0u);
+#pragma unroll 1
+  for (int i = 0; i < 16; ++i) {
+    if (!((which >> i) & 1u)) continue;
+    const float q[8] = {__fdiv_rn(v[i], d), 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    const uint32_t code = e2m1x8(q) & 0xFu;
+    const int sh = 4 * (i & 7);
+    if (i < 8)
+      c.x = (c.x & ~(0xFu << sh)) | (code << sh);
+    else
+      c.y = (c.y & ~(0xFu << sh)) | (code << sh);
+  }
+  return c;
+}
+
+// One bit per element whose 4-bit codes in a and b differ.
+__device__ __forceinline__ uint32_t nibble_mask(uint32_t x) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m |= ((x >> (4 * i)) & 0xFu) != 0u ? (1u << i) : 0u;
+  return m;
 }
 
 __device__ __forceinline__ uint2 block_codes(const float (&v)[16], float2 y, float ts, uint32_t sb) {
@@ -181,25 +202,15 @@ __device__ __forceinline__ uint2 block_codes(const float (&v)[16], float2 y, flo
     fmul2_rn(v[i], v[i + 1], y.y, y.y, ha[i], ha[i + 1]);
     fmul2_rn(v[8 + i], v[9 + i], y.y, y.y, hb[i], hb[i + 1]);
   }
-  uint2 c = make_uint2(e2m1x8(la), e2m1x8(lb));
+  const uint2 c = make_uint2(e2m1x8(la), e2m1x8(lb));
   const uint32_t dx = c.x ^ e2m1x8(ha), dy = c.y ^ e2m1x8(hb);
   const bool bracket_ok = y.y < 0x1p100f;
   if (bracket_ok && (dx | dy) == 0u) return c;
-  const float d = __fmul_rn(e4m3_to_float(sb), ts);
-  if (d == 0.0f) return make_uint2(0u, 0u);
+  float vv[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int sh = 4 * (i & 7);
-    const uint32_t differ = ((i < 8 ? dx : dy) >> sh) & 0xFu;
-    if (!bracket_ok || differ != 0u) {
-      const uint32_t code = code_by_division(v[i], d) << sh;
-      if (i < 8)
-        c.x = (c.x & ~(0xFu << sh)) | code;
-      else
-        c.y = (c.y & ~(0xFu << sh)) | code;
-    }
-  }
-  return c;
+  for (int i = 0; i < 16; ++i) vv[i] = v[i];
+  const uint32_t which = bracket_ok ? (nibble_mask(dx) | (nibble_mask(dy) << 8)) : 0xFFFFu;
+  return block_codes_slow(vv, __fmul_rn(e4m3_to_float(sb), ts), which, c);
 }
 
 __device__ __forceinline__ void load_scale16(const float* __restrict__ pqs, int b, float (&s)[16]) {
