@@ -67,6 +67,8 @@ typedef int32_t h3lin_status;
 #define H3LIN_E_CUDA        5  /* CUDA runtime error while enqueueing / no device     */
 #define H3LIN_E_TIMEOUT     6  /* device-side bounded wait expired (device status)    */
 #define H3LIN_E_UNSUPPORTED 7  /* device is not compute capability 10.x (tcgen05)     */
+#define H3LIN_E_BOUNDS      8  /* (device status, bounds build only) an index left its
+                                  buffer; the access was skipped                     */
 
 /* Output element types of h3lin_forward. */
 #define H3LIN_OUT_BF16      0  /* bf16, round to nearest even (the model's dtype)         */
@@ -369,6 +371,22 @@ h3lin_status h3lin_qk_norm_rope(void* qkv, int64_t M, const h3lin_rope_params* p
  * detection. */
 h3lin_status h3lin_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t wait_cycles,
                                          cudaStream_t stream);
+
+/* ------------------------------------------------------- bounds self-test */
+/* The bounds build of this library (libh3lin_bounds.so, compiled with
+ * -DH3LIN_BOUNDS) checks in its kernels the index of every plain global
+ * access that no TMA tensor map bounds; an index outside its buffer records
+ * H3LIN_E_BOUNDS in the workspace status word and the access is skipped, so
+ * a bad index is reported instead of corrupting memory or faulting.  This
+ * entry point proves the check is live: a kernel stores through an index
+ * past the end of a 16-byte window inside the workspace header (the store's
+ * address is still inside the workspace); the check must record
+ * H3LIN_E_BOUNDS and skip it.  In the normal build it returns
+ * H3LIN_E_UNSUPPORTED and enqueues nothing.  No counterpart in the paper:
+ * part of the library's memory-safety checks.
+ *   workspace  >= h3lin_quant_workspace_bytes(), initialised */
+h3lin_status h3lin_selftest_bounds(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int32_t      h3lin_bounds_build(void);   /* 1 in the bounds build, else 0 */
 
 /* ----------------------------------------------- forward without allocation */
 /* No counterpart in the paper: a library-level addition.

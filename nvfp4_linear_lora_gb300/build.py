@@ -19,6 +19,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libh3lin.so")
+# The bounds build: the same sources with -DH3LIN_BOUNDS, whose kernels check
+# every plain global index and report a bad one in the status word instead of
+# touching memory (see h3lin_selftest_bounds in include/h3lin.h).
+BOUNDS_LIB = os.path.join(PKG, "libh3lin_bounds.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -41,41 +45,45 @@ def _headers():
     return hs + [os.path.join(ROOT, "include", "h3lin.h")]
 
 
-def _compile(src, verbose_ptxas=False):
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [_nvcc()] + ARCH + FLAGS + (["-Xptxas", "-v"] if verbose_ptxas else []) + ["-c", src, "-o", obj]
+def _compile(src, build_dir, extra, verbose_ptxas=False):
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [_nvcc()] + ARCH + FLAGS + extra + (["-Xptxas", "-v"] if verbose_ptxas else []) + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
     return obj, r.stderr
 
 
-def needs_build():
-    if not os.path.exists(LIB):
+def needs_build(lib=LIB):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _sources() + _headers())
 
 
-def build(force=False, verbose_ptxas=False):
-    """Compile every CUDA source for sm_103a and link ``libh3lin.so``."""
-    if not force and not needs_build():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose_ptxas=False, bounds=False):
+    """Compile every CUDA source for sm_103a and link ``libh3lin.so`` (with
+    ``bounds``: ``libh3lin_bounds.so``, the bounds-checked build)."""
+    lib = BOUNDS_LIB if bounds else LIB
+    if not force and not needs_build(lib):
+        return lib
+    build_dir = os.path.join(BUILD, "bounds") if bounds else BUILD
+    extra = ["-DH3LIN_BOUNDS"] if bounds else []
+    os.makedirs(build_dir, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose_ptxas), _sources()))
+        results = list(ex.map(lambda s: _compile(s, build_dir, extra, verbose_ptxas), _sources()))
     if verbose_ptxas:
         for _, log in results:
             sys.stderr.write(log)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [_nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, bounds="--bounds" in sys.argv))

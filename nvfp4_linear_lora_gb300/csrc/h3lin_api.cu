@@ -2,6 +2,9 @@
 // before anything is enqueued), workspace layout, TMA tensor maps and the
 // kernel sequence.  See include/h3lin.h for the contract of every call.
 #include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -10,6 +13,26 @@
 #include "h3lin_internal.h"
 
 namespace h3lin {
+
+bool trace_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("H3LIN_TRACE");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+
+void trace_launch(const char* kernel, long grid, int cluster, int block, int smem, const char* fmt, ...) {
+  if (!trace_enabled()) return;
+  char detail[256];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(detail, sizeof(detail), fmt, ap);
+  va_end(ap);
+  std::fprintf(stderr, "h3lin: %s grid=%ld cluster=%d block=%d smem=%d %s\n", kernel, grid, cluster, block, smem,
+               detail);
+}
+
 namespace {
 
 constexpr int64_t kMaxDim = int64_t(1) << 30;   // rows, N
@@ -160,10 +183,12 @@ h3lin_status quantize_impl(const void* x, int64_t M, int64_t K, const float* pqs
   h3lin_status s = require_device(&d);
   if (s != H3LIN_OK) return s;
   float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kPartialsOffset);
+  uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + kStatusOffset);
   const RowPlan plan = plan_rows(M, K, d.sm_count);
-  if (launch_amax(x, int(M), int(K), pqs, partials, plan, nullptr, stream) != cudaSuccess) return H3LIN_E_CUDA;
+  if (launch_amax(x, int(M), int(K), pqs, partials, plan, nullptr, status, stream) != cudaSuccess)
+    return H3LIN_E_CUDA;
   if (launch_quant(x, int(M), int(K), pqs, partials, plan.blocks, nullptr, codes, scales, ts, plan, nullptr,
-                   nullptr, 0, 0.0f, nullptr, nullptr, 0, d.sm_count, stream) != cudaSuccess)
+                   nullptr, 0, 0.0f, nullptr, nullptr, 0, status, d.sm_count, stream) != cudaSuccess)
     return H3LIN_E_CUDA;
   return H3LIN_OK;
 }
@@ -274,13 +299,13 @@ h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
                          c.dev.sm_count, &nparts, stream) != cudaSuccess)
       return H3LIN_E_CUDA;
   } else if (!c.produced) {
-    if (launch_amax(c.x, int(c.M), int(c.K), c.pqs, partials, plan, nullptr, stream) != cudaSuccess)
+    if (launch_amax(c.x, int(c.M), int(c.K), c.pqs, partials, plan, nullptr, status, stream) != cudaSuccess)
       return H3LIN_E_CUDA;
   }
   if (launch_quant(c.x, int(c.M), int(c.K), c.pqs, partials, nparts, c.produced ? produced_count : nullptr, xq, xs,
                    ts_x, plan,
                    c.lora ? c.adapter->B : nullptr, c.lora ? bp : nullptr, c.lora ? c.N * c.rank : 0, lora_k,
-                   c.w->tensor_scale, c.lora ? u : nullptr, c.lora ? c.M * c.rank : 0, c.dev.sm_count,
+                   c.w->tensor_scale, c.lora ? u : nullptr, c.lora ? c.M * c.rank : 0, status, c.dev.sm_count,
                    stream) != cudaSuccess)
     return H3LIN_E_CUDA;
   return H3LIN_OK;
@@ -336,7 +361,8 @@ h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream, const Produ
   if (prod && !fused_amax) {
     const RowPlan plan = plan_rows(c.M, g.ldo, c.dev.sm_count);
     if (launch_amax(c.out, int(c.M), g.ldo, prod->pqs, reinterpret_cast<float*>(prod->ws + kPartialsOffset), plan,
-                    reinterpret_cast<int*>(prod->ws + kProducedOffset), stream) != cudaSuccess)
+                    reinterpret_cast<int*>(prod->ws + kProducedOffset),
+                    reinterpret_cast<uint32_t*>(prod->ws + kStatusOffset), stream) != cudaSuccess)
       return H3LIN_E_CUDA;
   }
   return H3LIN_OK;
@@ -360,7 +386,8 @@ const char* h3lin_status_string(h3lin_status s) {
     case H3LIN_E_WORKSPACE: return "workspace too small";
     case H3LIN_E_CUDA: return "CUDA error while enqueueing";
     case H3LIN_E_TIMEOUT: return "device-side wait timed out";
-    case H3LIN_E_UNSUPPORTED: return "device is not sm_103 (GB300)";
+    case H3LIN_E_UNSUPPORTED: return "device is not sm_103 (GB300), or the call is not in this build";
+    case H3LIN_E_BOUNDS: return "a kernel index left its buffer (bounds build; the access was skipped)";
     default: return "unknown status";
   }
 }

@@ -36,6 +36,21 @@ struct Abort {
   }
 };
 
+// ------------------------------------------------------------- bounds build
+// Built with -DH3LIN_BOUNDS (libh3lin_bounds.so), the kernels check the
+// index of every plain global access whose extent no TMA tensor map enforces:
+// an index outside its buffer records H3LIN_E_BOUNDS in the status word
+// (first error wins) and the access is skipped; nothing traps.  In the normal
+// build the check is the constant true and compiles away.
+#ifdef H3LIN_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, uint32_t* status) {
+  if (!ok && status != nullptr) atomicCAS(status, 0u, static_cast<uint32_t>(H3LIN_E_BOUNDS));
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, uint32_t*) { return true; }
+#endif
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

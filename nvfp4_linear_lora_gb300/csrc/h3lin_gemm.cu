@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
                 }
                 hv[e] = __fmul_rn(silu(g), u);
               }
-              store8<F32OUT>(out_row, col0 + 32 * i + 8 * w, hv);
+              if (in_bounds(col0 + 32 * i + 8 * w + 8 <= ldo, status)) store8<F32OUT>(out_row, col0 + 32 * i + 8 * w, hv);
             }
           }
         } else {
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_fp4gemm(
                 hv[e] = __fmul_rn(scale, __uint_as_float(v[i][8 * w + e]));
                 if (two) hv[e] = __fmul_rn(hv[e], post);
               }
-              store8<F32OUT>(out_row, col0 + 32 * i + 8 * w, hv);
+              if (in_bounds(col0 + 32 * i + 8 * w + 8 <= ldo, status)) store8<F32OUT>(out_row, col0 + 32 * i + 8 * w, hv);
             }
           }
         }
@@ -327,6 +327,9 @@ static cudaError_t launch_variant(const GemmArgs& a, int sm_count, cudaStream_t 
   const int tiles_n = SILU ? (a.N / 2) / 128 : a.N / BN;
   const int tiles = tiles_m * tiles_n;
   const int grid = tiles < sm_count ? tiles : sm_count;
+  trace_launch("k_fp4gemm", grid, 1, kGemmThreads, C::kSmem, "BN=%d silu=%d lora=%d f32out=%d M=%d N=%d K=%d rank=%d "
+               "tiles=%d raster_group=%d", BN, int(SILU), int(LORA), int(F32OUT), a.M, a.N, a.K, a.rank, tiles,
+               a.group_m);
   kern<<<grid, kGemmThreads, C::kSmem, st>>>(a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.xs, a.ws, a.ts_x, a.ts_w,
                                              a.out, a.M, a.N, a.K, a.rank, a.ldo, a.group_m,
                                              a.status);
@@ -710,7 +713,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
           epi_convert<SILU, F32OUT, true>(scale, post, a, b, rd, w);
         else
           epi_convert<SILU, F32OUT, false>(scale, 1.0f, a, b, rd, w);
-        if (AMAX && row0 + lane < M) {
+        if (AMAX && row0 + lane < M && in_bounds(col0 + rd * kRoundCols + kRoundCols <= ldo, status)) {
           // per element: |fl(h * s)| with h the stored bf16 value (the lanes'
           // loads of s are broadcasts: all lanes read the same 32 columns)
           const int cb = col0 + rd * kRoundCols;
@@ -744,7 +747,7 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
   if (AMAX && threadIdx.x == 0) {
     float m = amax_red[0];
     for (int i = 1; i < C::kEpiWarps; ++i) m = fmaxf(m, amax_red[i]);
-    amax_out[blockIdx.x] = m;
+    if (in_bounds(blockIdx.x < static_cast<unsigned>(kMaxPartials), status)) amax_out[blockIdx.x] = m;
     if (blockIdx.x == 0) *amax_count = static_cast<int>(gridDim.x);
   }
   cluster_sync_all();
@@ -776,6 +779,9 @@ static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStre
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  trace_launch("k_fp4gemm_pair", grid, 2, PairRoles<SILU>::kThreads, PairCfg::kSmem,
+               "silu=%d lora=%d f32out=%d amax=%d M=%d N=%d K=%d rank=%d tiles=%d raster_group=%d", int(SILU),
+               int(LORA), int(F32OUT), int(AMAX), a.M, a.N, a.K, a.rank, tiles, a.group_m);
   return cudaLaunchKernelEx(&cfg, kern, a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.tm_xs, a.tm_ws, a.tm_out, a.ts_x, a.ts_w,
                             a.out, a.M, a.N, a.K, a.rank, a.ldo, a.group_m, a.status, a.amax_s, a.amax_out,
                             a.amax_count);

@@ -24,6 +24,13 @@ constexpr size_t kRegionAlign = 1024;
 
 constexpr int kQuantThreads = 256;
 
+// Launch tracing: with the environment variable H3LIN_TRACE set (to anything
+// but "0"), every kernel launch is described on one stderr line before it is
+// enqueued: kernel and variant, grid, cluster, block, dynamic shared memory,
+// problem sizes and launch plan.  Read once per process (h3lin_api.cu).
+bool trace_enabled();
+void trace_launch(const char* kernel, long grid, int cluster, int block, int smem, const char* fmt, ...);
+
 // Launch plans computed on the host.
 struct RowPlan {   // k_amax / k_quant: each thread owns one 16-byte column chunk
   int blocks;      // grid size
@@ -34,7 +41,7 @@ RowPlan plan_rows(int64_t M, int64_t K, int sm_count);
 // Kernel launchers (enqueue only; arguments already validated).
 // count_out (nullable): block 0 writes the number of partials there.
 cudaError_t launch_amax(const void* x, int M, int K, const float* pqs, float* partials, const RowPlan& p,
-                        int* count_out, cudaStream_t st);
+                        int* count_out, uint32_t* status, cudaStream_t st);
 // nparts_dev (nullable): the kernel reads the number of partials there instead
 // of taking nparts (partials left by a producer GEMM).
 cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
@@ -42,7 +49,7 @@ cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const fl
                          // optional: B' = bf16(B * lora_k / (ts * ts_w)), elems % 8 == 0; u (bf16,
                          // written by the amax pass) takes a power of two from B' for tiny tensor scales
                          const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
-                         void* u, int64_t u_elems, int sm_count, cudaStream_t st);
+                         void* u, int64_t u_elems, uint32_t* status, int sm_count, cudaStream_t st);
 // amax pass fused with u = A(x) (bf16 [M, rank]); returns grid size in *nparts.
 cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
                              int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,

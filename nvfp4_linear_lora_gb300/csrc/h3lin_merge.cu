@@ -98,6 +98,7 @@ cudaError_t launch_merge_lora(const void* w, const void* A, const void* B, const
                               int K, int rank, float c, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>((K + kMergeCols - 1) / kMergeCols),
                   static_cast<unsigned>((N + kMergeRows - 1) / kMergeRows));
+  trace_launch("k_merge_lora", long(grid.x) * grid.y, 1, kMergeThreads, 0, "N=%d K=%d rank=%d", N, K, rank);
   k_merge_lora<<<grid, kMergeThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(w),
                                                    static_cast<const __nv_bfloat16*>(A),
                                                    static_cast<const __nv_bfloat16*>(B), pqs,

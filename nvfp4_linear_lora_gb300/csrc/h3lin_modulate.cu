@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kModThreads) k_modulate(const uint4* __restric
         for (int k = 0; k < 8; ++k) o[k] = bad ? 0.0f : fmaf((v[k] - mean) * rstd, 1.0f + sc[k], sh[k]);
         const uint4 r = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                                    pack_bf16x2(o[6], o[7]));
-        out[int64_t(row) * kc + c] = r;
+        if (in_bounds(row < M && c < kc, status)) out[int64_t(row) * kc + c] = r;
         const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -163,6 +163,7 @@ static cudaError_t launch_cpt(const void* x, int M, int K, const float* table, i
   int grid = (per_sm > 0 ? per_sm : 1) * sm_count;
   if (grid > M) grid = M;
   if (grid > kMaxPartials) grid = kMaxPartials;
+  trace_launch("k_modulate", grid, 1, kModThreads, 0, "M=%d K=%d chunks_per_thread=%d table_rows=%d", M, K, CPT, T);
   k_modulate<CPT><<<grid, kModThreads, 0, st>>>(static_cast<const uint4*>(x), M, K, table, T, row_table, eps,
                                                 static_cast<uint4*>(out), pqs, partials, count, status);
   return cudaGetLastError();

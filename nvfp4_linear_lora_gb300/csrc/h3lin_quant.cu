@@ -89,7 +89,7 @@ __device__ __forceinline__ float block_max(float m, float* red) {
 __global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict__ x, int M, int kc,
                                                        const float* __restrict__ pqs,
                                                        float* __restrict__ partials, int rows_step,
-                                                       int* __restrict__ count_out) {
+                                                       int* __restrict__ count_out, uint32_t* status) {
   __shared__ float red[kQuantThreads / 32];
   const int tid = blockIdx.x * kQuantThreads + threadIdx.x;
   const int c = tid % kc;
@@ -98,19 +98,23 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax(const uint4* __restrict_
   if (r0 < rows_step) {
     ColMax8 cm;
     int row = r0;
+    const int64_t x_chunks = static_cast<int64_t>(M) * kc;
     for (; row + rows_step < M; row += 2 * rows_step) {
-      const uint4 a = x[static_cast<int64_t>(row) * kc + c];
-      const uint4 b = x[static_cast<int64_t>(row + rows_step) * kc + c];
+      const int64_t ia = static_cast<int64_t>(row) * kc + c, ib = static_cast<int64_t>(row + rows_step) * kc + c;
+      if (!in_bounds(ia < x_chunks && ib < x_chunks, status)) break;
+      const uint4 a = x[ia];
+      const uint4 b = x[ib];
       cm.add(a);
       cm.add(b);
     }
-    if (row < M) cm.add(x[static_cast<int64_t>(row) * kc + c]);
+    if (row < M && in_bounds(static_cast<int64_t>(row) * kc + c < x_chunks, status))
+      cm.add(x[static_cast<int64_t>(row) * kc + c]);
     float s[8];
     load_scale8(pqs, c, s);
     m = cm.scaled_max(s);
   }
   m = block_max(m, red);
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && in_bounds(blockIdx.x < static_cast<unsigned>(kMaxPartials), status)) {
     partials[blockIdx.x] = m;
     if (count_out && blockIdx.x == 0) *count_out = static_cast<int>(gridDim.x);
   }
@@ -286,12 +290,13 @@ __global__ void __launch_bounds__(kQuantThreads, 4) k_quant(
     const float* __restrict__ partials, int nparts, const int* __restrict__ nparts_dev, uint2* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ ts_out, int rows_step, const uint4* __restrict__ b_src,
     uint4* __restrict__ b_dst, int64_t b_chunks, float lora_k, const float* __restrict__ ts_w, uint4* u,
-    int64_t u_chunks) {
+    int64_t u_chunks, uint32_t* status) {
   __shared__ float red[kQuantThreads / 32];
   __shared__ float2 yt[256];
   float m = 0.0f;
   if (nparts_dev) nparts = min(max(*nparts_dev, 0), kMaxPartials);   // never read past the partials
-  for (int i = threadIdx.x; i < nparts; i += kQuantThreads) m = fmaxf(m, partials[i]);
+  for (int i = threadIdx.x; i < nparts; i += kQuantThreads)
+    if (in_bounds(i < kMaxPartials, status)) m = fmaxf(m, partials[i]);
   const float amax = block_max(m, red);
   float ts = __fdiv_rn(amax, 2688.0f);
   if (ts == 0.0f) ts = 1.0f;
@@ -313,19 +318,26 @@ __global__ void __launch_bounds__(kQuantThreads, 4) k_quant(
       const bool has_b = i + rows_step < Mpad;
       const int rb = Mpad - 1 - (i + rows_step);
       uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, c0 = a0, c1 = a0;
-      if (ra < M) {
+      // bounds build: x chunks, code words and scale bytes against their buffers
+      const int64_t x_chunks = static_cast<int64_t>(M) * kc, code_words = static_cast<int64_t>(M) * kb;
+      const int64_t sf_bytes = static_cast<int64_t>(Mpad) * kb;
+      if (ra < M && in_bounds(static_cast<int64_t>(ra) * kc + 2 * b + 1 < x_chunks, status)) {
         const uint4* p = x + static_cast<int64_t>(ra) * kc + 2 * b;
         a0 = __ldcs(p);
         a1 = __ldcs(p + 1);
       }
-      if (has_b && rb < M) {
+      if (has_b && rb < M && in_bounds(static_cast<int64_t>(rb) * kc + 2 * b + 1 < x_chunks, status)) {
         const uint4* p = x + static_cast<int64_t>(rb) * kc + 2 * b;
         c0 = __ldcs(p);
         c1 = __ldcs(p + 1);
       }
-      if (ra < M) quant_block(q, codes + static_cast<int64_t>(ra) * kb + b, scales + sf_offset(ra, b, K), a0, a1, s);
-      else scales[sf_offset(ra, b, K)] = 0;
-      if (has_b) {
+      if (in_bounds(ra >= 0 && sf_offset(ra, b, K) < sf_bytes && (ra >= M || static_cast<int64_t>(ra) * kb + b < code_words),
+                    status)) {
+        if (ra < M) quant_block(q, codes + static_cast<int64_t>(ra) * kb + b, scales + sf_offset(ra, b, K), a0, a1, s);
+        else scales[sf_offset(ra, b, K)] = 0;
+      }
+      if (has_b && in_bounds(rb >= 0 && sf_offset(rb, b, K) < sf_bytes &&
+                             (rb >= M || static_cast<int64_t>(rb) * kb + b < code_words), status)) {
         if (rb < M) quant_block(q, codes + static_cast<int64_t>(rb) * kb + b, scales + sf_offset(rb, b, K), c0, c1, s);
         else scales[sf_offset(rb, b, K)] = 0;
       }
@@ -399,7 +411,8 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
   if (QUANT) {   // tensor amax from the producer's partials (every CTA, deterministic)
     const int n = min(max(*qo.nparts_dev, 0), kMaxPartials);   // never read past the partials
     float m = 0.0f;
-    for (int i = threadIdx.x; i < n; i += kThreads) m = fmaxf(m, qo.partials_in[i]);
+    for (int i = threadIdx.x; i < n; i += kThreads)
+      if (in_bounds(i < kMaxPartials, status)) m = fmaxf(m, qo.partials_in[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (lane == 0) red[warp] = m;
@@ -565,8 +578,9 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
             const uint4 w0 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj) ^ (r & 7)) << 4));
             const uint4 w1 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj + 1) ^ (r & 7)) << 4));
             // rows >= M were filled with zeros by the TMA load: scale 0, no codes
-            quant_block(qc, code_row[h] ? code_row[h] + 4 * kc : nullptr, sf_tile + kc * 512 + sf_in_atom[h], w0, w1,
-                        qs);
+            if (in_bounds((t * 128 + 128 <= ((M + 127) & ~127)) && 4 * kc + 3 < (K >> 4), status))
+              quant_block(qc, code_row[h] ? code_row[h] + 4 * kc : nullptr, sf_tile + kc * 512 + sf_in_atom[h], w0,
+                          w1, qs);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[st]);
@@ -606,9 +620,9 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           tmem_ld_wait();
-          if (row < M) {
+          const int nvec = (rank - c0) >= 32 ? 4 : 2;
+          if (row < M && in_bounds(row >= 0 && c0 + 8 * nvec <= rank, status)) {
             uint4* dst = reinterpret_cast<uint4*>(u + static_cast<int64_t>(row) * rank + c0);
-            const int nvec = (rank - c0) >= 32 ? 4 : 2;
             for (int v = 0; v < nvec; ++v) {
               float f[8];
 #pragma unroll
@@ -640,7 +654,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
   }
   tc_fence_before();
   __syncthreads();
-  if (!QUANT && threadIdx.x == 0) {
+  if (!QUANT && threadIdx.x == 0 && in_bounds(blockIdx.x < static_cast<unsigned>(kMaxPartials), status)) {
     float m = red[0];
     for (int i = 1; i < kLoraAmaxWarps; ++i) m = fmaxf(m, red[i]);
     partials[blockIdx.x] = m;
@@ -668,9 +682,10 @@ RowPlan plan_rows(int64_t M, int64_t K, int sm_count) {
 }
 
 cudaError_t launch_amax(const void* x, int M, int K, const float* pqs, float* partials, const RowPlan& p,
-                        int* count_out, cudaStream_t st) {
+                        int* count_out, uint32_t* status, cudaStream_t st) {
+  trace_launch("k_amax", p.blocks, 1, kQuantThreads, 0, "M=%d K=%d rows_step=%d", M, K, p.rows_step);
   k_amax<<<p.blocks, kQuantThreads, 0, st>>>(static_cast<const uint4*>(x), M, K / 8, pqs, partials, p.rows_step,
-                                             count_out);
+                                             count_out, status);
   return cudaGetLastError();
 }
 
@@ -699,13 +714,15 @@ static RowPlan plan_quant(int64_t M, int64_t K, int sm_count) {
 cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const float* partials, int nparts,
                          const int* nparts_dev, void* codes, void* scales, float* ts_out, const RowPlan& /*amax plan*/,
                          const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
-                         void* u, int64_t u_elems, int sm_count, cudaStream_t st) {
+                         void* u, int64_t u_elems, uint32_t* status, int sm_count, cudaStream_t st) {
   const int Mpad = ((M + 127) / 128) * 128;
   const RowPlan p = plan_quant(M, K, sm_count);
+  trace_launch("k_quant", p.blocks, 1, kQuantThreads, 0, "M=%d K=%d rows_step=%d lora_b=%lld", M, K, p.rows_step,
+               static_cast<long long>(b_elems));
   k_quant<<<p.blocks, kQuantThreads, 0, st>>>(
       static_cast<const uint4*>(x), M, Mpad, K, pqs, partials, nparts, nparts_dev, static_cast<uint2*>(codes),
       static_cast<uint8_t*>(scales), ts_out, p.rows_step, static_cast<const uint4*>(b_src),
-      static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w, static_cast<uint4*>(u), u_elems / 8);
+      static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w, static_cast<uint4*>(u), u_elems / 8, status);
   return cudaGetLastError();
 }
 
@@ -733,6 +750,8 @@ static cudaError_t launch_lora_pass(const CUtensorMap& tm_x, const CUtensorMap& 
   if (grid > kMaxPartials) grid = kMaxPartials;
   cudaError_t e = cudaFuncSetAttribute(k_amax_lora<QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  trace_launch(QUANT ? "k_amax_lora<quant>" : "k_amax_lora<amax>", grid, 1, lora_threads<QUANT>(), smem,
+               "M=%d K=%d rank=%d stages=%d ctas_per_sm=%d tmem_cols=%d", M, K, rank, stages, two ? 2 : 1, tmem_cols);
   k_amax_lora<QUANT><<<grid, lora_threads<QUANT>(), smem, st>>>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, partials,
                                                        static_cast<__nv_bfloat16*>(u), status, stages, tmem_cols, qo);
   if (grid_out) *grid_out = grid;

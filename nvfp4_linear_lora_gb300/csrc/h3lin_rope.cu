@@ -140,9 +140,10 @@ __global__ void __launch_bounds__(kRopeThreads, 2) k_qk_norm_rope(__nv_bfloat16*
         for (int k = 0; k < 8; ++k) pv[k] = __shfl_sync(0xFFFFFFFFu, y[k], partner, 16);
 #pragma unroll
         for (int k = 0; k < 8; ++k) o[k] = fmaf(pv[k], s8[k], y[k] * c8[k]);
-        *reinterpret_cast<uint4*>(out + int64_t(hv) * 128) =
-            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
-                       pack_bf16x2(o[6], o[7]));
+        if (in_bounds(row < M && hv < nhv && d0 + 8 <= 128, status))
+          *reinterpret_cast<uint4*>(out + int64_t(hv) * 128) =
+              make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                         pack_bf16x2(o[6], o[7]));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
@@ -179,6 +180,7 @@ cudaError_t launch_qk_norm_rope(void* qkv, int M, int heads, int rot, const int 
   if (e != cudaSuccess) return e;
   int grid = (budget == kRopeCtaSmem ? 2 : 1) * sm_count;
   if (grid > M) grid = M;
+  trace_launch("k_qk_norm_rope", grid, 1, kRopeThreads, smem, "M=%d heads=%d rot=%d", M, heads, rot);
   k_qk_norm_rope<<<grid, kRopeThreads, smem, st>>>(static_cast<__nv_bfloat16*>(qkv), M, heads, rot / 2, eps, q_gain,
                                                    k_gain, pos, status, stages, f);
   return cudaGetLastError();

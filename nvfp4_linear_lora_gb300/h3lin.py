@@ -14,7 +14,17 @@ import os
 from dataclasses import dataclass
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libh3lin.so")
+# H3LIN_BOUNDS=1 loads the bounds-checked build (libh3lin_bounds.so: every
+# plain global index checked in the kernels, a bad one reported in the
+# workspace status word as H3LIN_E_BOUNDS instead of touching memory).
+BOUNDS = os.environ.get("H3LIN_BOUNDS") == "1"
+LIB_PATH = os.path.join(_HERE, "libh3lin_bounds.so" if BOUNDS else "libh3lin.so")
+# H3LIN_CANARY=1 gives every workspace and output the helpers below allocate a
+# guard region of CANARY_BYTES filled with CANARY_BYTE right after it;
+# check_canaries() verifies that no kernel wrote past a buffer's end.
+CANARY = os.environ.get("H3LIN_CANARY") == "1"
+CANARY_BYTES = 4096
+CANARY_BYTE = 0xA5
 
 H3LIN_OK = 0
 H3LIN_E_INVALID = 1
@@ -24,6 +34,7 @@ H3LIN_E_WORKSPACE = 4
 H3LIN_E_CUDA = 5
 H3LIN_E_TIMEOUT = 6
 H3LIN_E_UNSUPPORTED = 7
+H3LIN_E_BOUNDS = 8
 H3LIN_OUT_BF16 = 0
 H3LIN_OUT_F32 = 1
 H3LIN_EPI_NONE = 0
@@ -83,6 +94,8 @@ _SIGNATURES = {
     "h3lin_modulate_produce": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "h3lin_selftest_wait_timeout": (_i32, [_vp, _sz, _i64, _vp]),
+    "h3lin_selftest_bounds": (_i32, [_vp, _sz, _vp]),
+    "h3lin_bounds_build": (_i32, []),
     "h3lin_merge_lora": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(h3lin_adapter), _f32, _vp, _vp]),
     "h3lin_forward_noalloc": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), _i32,
                                      ctypes.POINTER(h3lin_adapter), _f32, _vp, _i32, _vp]),
@@ -97,7 +110,8 @@ def lib():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with nvfp4_linear_lora_gb300.build.build()")
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with nvfp4_linear_lora_gb300.build.build()"
+                               + (" (bounds=True)" if BOUNDS else ""))
         L = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in _SIGNATURES.items():
             fn = getattr(L, name)
@@ -230,6 +244,14 @@ def h3lin_selftest_wait_timeout(ws, ws_bytes, wait_cycles, stream):
     return lib().h3lin_selftest_wait_timeout(ws, ws_bytes, wait_cycles, stream)
 
 
+def h3lin_selftest_bounds(ws, ws_bytes, stream):
+    return lib().h3lin_selftest_bounds(ws, ws_bytes, stream)
+
+
+def h3lin_bounds_build():
+    return lib().h3lin_bounds_build()
+
+
 def h3lin_read_status(ws, stream):
     v = _i32(-1)
     st = lib().h3lin_read_status(ws, stream, ctypes.byref(v))
@@ -282,9 +304,62 @@ class Adapter:
         return h3lin_adapter(self.A.data_ptr(), self.B.data_ptr(), self.rank, self.alpha)
 
 
+_guards = []   # (guard tensor, where) of the buffers allocated with a canary tail
+
+
+def _alloc(shape, dtype, device):
+    """torch.empty, or (with H3LIN_CANARY=1) a view of a larger buffer whose
+    CANARY_BYTES-long tail is filled with CANARY_BYTE and remembered."""
+    torch = _torch()
+    if not CANARY:
+        return torch.empty(shape, dtype=dtype, device=device)
+    n = 1
+    for d in shape:
+        n *= int(d)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    raw = torch.empty(nbytes + CANARY_BYTES, dtype=torch.uint8, device=device)
+    raw[nbytes:].fill_(CANARY_BYTE)
+    _guards.append((raw[nbytes:], f"{tuple(shape)} {dtype}"))
+    return raw[:nbytes].view(dtype).view(shape)
+
+
+def check_canaries():
+    """Raise if a kernel wrote into the guard tail of any buffer allocated
+    since the last check (H3LIN_CANARY=1 only); forget those buffers."""
+    global _guards
+    if not CANARY:
+        return
+    torch = _torch()
+    torch.cuda.synchronize()
+    bad = [where for g, where in _guards if not bool((g == CANARY_BYTE).all())]
+    _guards = []
+    if bad:
+        raise AssertionError(f"canary overwritten after: {bad}")
+
+
+_bounds_ws = []   # bounds build: the workspaces whose status words check_bounds_status() reads
+
+
+def check_bounds_status():
+    """Bounds build only: raise if any workspace allocated since the last check
+    recorded H3LIN_E_BOUNDS (a kernel index left its buffer); forget them."""
+    global _bounds_ws
+    if not BOUNDS:
+        return
+    torch = _torch()
+    torch.cuda.synchronize()
+    hit = [int(w.numel()) for w in _bounds_ws
+           if int(w[:4].view(torch.int32).item()) == H3LIN_E_BOUNDS]
+    _bounds_ws = []
+    if hit:
+        raise AssertionError(f"H3LIN_E_BOUNDS recorded in workspaces of {hit} bytes")
+
+
 def new_workspace(nbytes, device="cuda"):
     torch = _torch()
-    ws = torch.empty(int(nbytes), dtype=torch.uint8, device=device)
+    ws = _alloc((int(nbytes),), torch.uint8, device)
+    if BOUNDS:
+        _bounds_ws.append(ws)
     _check(h3lin_workspace_init(ws.data_ptr(), ws.numel(), _stream()), "h3lin_workspace_init")
     return ws
 
@@ -293,9 +368,9 @@ def quantize_act(x, pre_quant_scale=None, workspace=None):
     """x bf16 [M, K] (cuda) -> (codes u8 [M, K/2], native scales u8, tensor scale f32 [1])."""
     torch = _torch()
     M, K = x.shape
-    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
-    scales = torch.empty(h3lin_scales_bytes(M, K), dtype=torch.uint8, device=x.device)
-    ts = torch.empty(1, dtype=torch.float32, device=x.device)
+    codes = _alloc((M, K // 2), torch.uint8, x.device)
+    scales = _alloc((h3lin_scales_bytes(M, K),), torch.uint8, x.device)
+    ts = _alloc((1,), torch.float32, x.device)
     ws = workspace if workspace is not None else new_workspace(h3lin_quant_workspace_bytes(), x.device)
     _check(h3lin_quantize_act(x.data_ptr(), M, K, _ptr(pre_quant_scale), codes.data_ptr(), scales.data_ptr(),
                               ts.data_ptr(), ws.data_ptr(), ws.numel(), _stream()), "h3lin_quantize_act")
@@ -306,9 +381,9 @@ def pack_weight(w, workspace=None):
     """w bf16 [N, K] (cuda) -> PackedWeight."""
     torch = _torch()
     N, K = w.shape
-    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
-    scales = torch.empty(h3lin_scales_bytes(N, K), dtype=torch.uint8, device=w.device)
-    ts = torch.empty(1, dtype=torch.float32, device=w.device)
+    codes = _alloc((N, K // 2), torch.uint8, w.device)
+    scales = _alloc((h3lin_scales_bytes(N, K),), torch.uint8, w.device)
+    ts = _alloc((1,), torch.float32, w.device)
     ws = workspace if workspace is not None else new_workspace(h3lin_quant_workspace_bytes(), w.device)
     _check(h3lin_pack_weight(w.data_ptr(), N, K, codes.data_ptr(), scales.data_ptr(), ts.data_ptr(),
                              ws.data_ptr(), ws.numel(), _stream()), "h3lin_pack_weight")
@@ -323,7 +398,7 @@ def forward(x, weight, pre_quant_scale=None, adapter=None, strength=1.0, silu_mu
     M = x.shape[0]
     n_out = weight.N // 2 if silu_mul else weight.N
     if out is None:
-        out = torch.empty((M, n_out), dtype=out_dtype or torch.bfloat16, device=x.device)
+        out = _alloc((M, n_out), out_dtype or torch.bfloat16, x.device)
     if out.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("out must be bfloat16 or float32")
     code = H3LIN_OUT_F32 if out.dtype == torch.float32 else H3LIN_OUT_BF16
@@ -347,9 +422,9 @@ def mlp_forward(x, gate_up, down, gate_up_pre_quant_scale=None, down_pre_quant_s
     torch = _torch()
     M = x.shape[0]
     if h is None:
-        h = torch.empty((M, gate_up.N // 2), dtype=torch.bfloat16, device=x.device)
+        h = _alloc((M, gate_up.N // 2), torch.bfloat16, x.device)
     if out is None:
-        out = torch.empty((M, down.N), dtype=out_dtype or torch.bfloat16, device=x.device)
+        out = _alloc((M, down.N), out_dtype or torch.bfloat16, x.device)
     if out.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("out must be bfloat16 or float32")
     code = H3LIN_OUT_F32 if out.dtype == torch.float32 else H3LIN_OUT_BF16
@@ -394,7 +469,7 @@ def modulate_produce(x, table, row_table, next_workspace, next_pre_quant_scale=N
     torch = _torch()
     M, K = x.shape
     if out is None:
-        out = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+        out = _alloc((M, K), torch.bfloat16, x.device)
     _check(h3lin_modulate_produce(x.data_ptr(), M, K, table.data_ptr(), table.shape[0], row_table.data_ptr(),
                                   float(eps), out.data_ptr(), _ptr(next_pre_quant_scale), next_workspace.data_ptr(),
                                   next_workspace.numel(), _stream()), "h3lin_modulate_produce")
@@ -410,7 +485,7 @@ def forward_produced(x, weight, workspace, pre_quant_scale=None, adapter=None, s
     M = x.shape[0]
     n_out = weight.N // 2 if silu_mul else weight.N
     if out is None:
-        out = torch.empty((M, n_out), dtype=out_dtype or torch.bfloat16, device=x.device)
+        out = _alloc((M, n_out), out_dtype or torch.bfloat16, x.device)
     code = H3LIN_OUT_F32 if out.dtype == torch.float32 else H3LIN_OUT_BF16
     wc = weight.c_struct()
     ac = adapter.c_struct() if adapter is not None else None
@@ -429,7 +504,7 @@ def merge_lora(w, adapter, strength=1.0, pre_quant_scale=None, out=None):
     if w.dtype != torch.bfloat16 or w.dim() != 2:
         raise TypeError("w must be a 2-D bfloat16 tensor")
     if out is None:
-        out = torch.empty_like(w)
+        out = _alloc(tuple(w.shape), w.dtype, w.device)
     _check(h3lin_merge_lora(w.data_ptr(), w.shape[0], w.shape[1], _ptr(pre_quant_scale), adapter.c_struct(),
                             float(strength), out.data_ptr(), _stream()), "h3lin_merge_lora")
     return out

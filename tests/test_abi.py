@@ -285,3 +285,22 @@ def test_noalloc_host_checks():
     # the projection the GPU test of this entry point runs fits in the scratch
     fits = h3lin.h3lin_forward_workspace_bytes(1024, 1024, 1280, 128)
     assert 0 < fits <= h3lin.H3LIN_NOALLOC_SCRATCH_BYTES
+
+
+def test_bounds_build_links_exports_and_reports_itself():
+    """The bounds-checked build compiles, exports every declared entry point
+    and says it is the bounds build; the normal build refuses the bounds
+    self-test on the host, before touching any device."""
+    import subprocess
+    import sys
+    from nvfp4_linear_lora_gb300 import build as h3build
+    path = h3build.build(bounds=True)
+    assert os.path.exists(path)
+    code = ("import ctypes; L = ctypes.CDLL(%r); "
+            "names = %r; missing = [n for n in names if not hasattr(L, n)]; "
+            "assert not missing, missing; print(L.h3lin_bounds_build())") % (path, _declared_functions())
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "1", r.stdout + r.stderr
+    assert h3lin.h3lin_bounds_build() == 0
+    assert h3lin.h3lin_selftest_bounds(A, 1 << 20, None) == h3lin.H3LIN_E_UNSUPPORTED
+    assert h3lin.h3lin_status_string(h3lin.H3LIN_E_BOUNDS).startswith("a kernel index")
