@@ -646,6 +646,61 @@ def reference_arm(a, rank, world):
     return 0
 
 
+def fused_qkv_rope_line(blk, wq, wk, pos, c, a, qkv_gemm_ms, rope_ms):
+    """The QKV GEMM stage with Q/K RMSNorm + RoPE in its epilogue
+    (h3lin_forward_gemm_qk_rope: the angle-table pass + the GEMM) on the
+    block's prepared QKV workspace, timed like the plain stage, against that
+    stage + the separate in-place pass; its output is checked bit for bit
+    against the two-step result on the same inputs."""
+    import torch
+    h = blk.h3lin
+    d = blk.proj[0]
+    S = blk.S
+    prm = h.rope_params(c["heads"], 128, c["rot"], c["axis_dims"], c["theta"], c["eps"])
+    wsb = h.h3lin_forward_qk_rope_workspace_bytes(S, d["K"], d["N"], d["rank"])
+    ws = h.new_workspace(wsb)
+    out = torch.empty_like(d["out"])
+    ref = torch.empty_like(d["out"])
+    st = d["stream"]
+
+    def check(code, what):
+        if code:
+            raise h.H3linError(code, what)
+
+    check(h.h3lin_forward_prepare(d["x_dev"].data_ptr(), S, d["pqs_dev"].data_ptr(), d["wc"], d["ac"], 1.0,
+                                  ws.data_ptr(), ws.numel(), st), "h3lin_forward_prepare")
+
+    def fused():
+        check(h.h3lin_forward_gemm_qk_rope(S, d["wc"], d["ac"], 1.0, prm, wq.data_ptr(), wk.data_ptr(), pos.data_ptr(),
+                                           out.data_ptr(), ws.data_ptr(), ws.numel(), st), "h3lin_forward_gemm_qk_rope")
+
+    for _ in range(max(3, a.warmup)):
+        fused()
+    n = max(10, a.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(n):
+        fused()
+    e1.record()
+    torch.cuda.synchronize()
+    fms = e0.elapsed_time(e1) / n
+    # the two-step result on the same workspace
+    check(h.h3lin_forward_gemm(S, d["wc"], 0, d["ac"], 1.0, ref.data_ptr(), h.H3LIN_OUT_BF16, ws.data_ptr(),
+                               ws.numel(), st), "h3lin_forward_gemm")
+    h.qk_norm_rope(ref, wq, wk, pos, c["heads"], c["rot"], c["axis_dims"], c["theta"], c["eps"], workspace=ws)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(out.view(torch.int16), ref.view(torch.int16)))
+    if h.read_status(ws) != 0:
+        raise RuntimeError("device status set by h3lin_forward_gemm_qk_rope")
+    del ws, out, ref
+    return {"ms": fms, "launches": 2 * n, "qkv_gemm_ms": qkv_gemm_ms, "qk_norm_rope_ms": rope_ms,
+            "two_step_ms": qkv_gemm_ms + rope_ms, "saved_ms": qkv_gemm_ms + rope_ms - fms,
+            "bit_identical_to_two_step": same,
+            "what": "h3lin_forward_gemm_qk_rope on the block's QKV (angle table + pair GEMM whose epilogue "
+                    "normalises and rotates Q and K before the store) vs the plain QKV GEMM + h3lin_qk_norm_rope"}
+
+
 def native_arm(a, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -732,6 +787,7 @@ def native_arm(a, rank, world, local_rank):
                      "what": "h3lin_qk_norm_rope in place on the block's QKV output [S, 15360] bf16: per-head "
                              "RMSNorm of Q and K, split-half RoPE of 96 of 128 dims over (t, h, w) positions; "
                              "bytes = Q and K read and written once + positions"}
+        rope_line["fused_in_qkv_gemm"] = fused_qkv_rope_line(blk, wq, wk, pos, c, a, gemm_ms[0], rms)
 
     # the step before QKV: the modulation producer (LayerNorm + segment-wise
     # AdaLN shift/scale -> bf16 LoRA input + amax partials), then QKV's prepare

@@ -359,6 +359,45 @@ h3lin_status h3lin_qk_norm_rope(void* qkv, int64_t M, const h3lin_rope_params* p
                                 const float* k_gain, const int32_t* positions, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------- QKV projection with Q/K RMSNorm + RoPE in its epilogue */
+/* The fused QKV projection and the Q/K RMSNorm + split-half RoPE step in one
+ * GEMM (MiniMax-H3 Ultra Fast README, "Active optimization stack", row
+ * "Attention projections"; "Kernel path", item 2): the GEMM's epilogue
+ * normalises and rotates every Q and K head of its tile before the single
+ * bf16 store, so Q and K are not read back and written again.  The result is
+ * bit-identical to
+ *     h3lin_forward(x, M, pre_quant_scale, weight, H3LIN_EPI_NONE, adapter,
+ *                   strength, out, H3LIN_OUT_BF16, ...)
+ *     h3lin_qk_norm_rope(out, M, params, q_gain, k_gain, positions, ...)
+ * and out holds the same [Q | K | V] rows; the arguments mean what they mean
+ * there.  A small pass first writes the (cos, sin) of every row's 48 rotation
+ * pairs into the workspace (angles as h3lin_qk_norm_rope computes them).
+ *   workspace  >= h3lin_forward_qk_rope_workspace_bytes(M, K, N, rank):
+ *              h3lin_forward's regions plus M * 384 bytes of angles;
+ *              initialised once (h3lin_workspace_init); its status word
+ *              records a timed-out device wait
+ * Rules: those of h3lin_forward and of h3lin_qk_norm_rope, and weight->N ==
+ * 3 * heads * head_dim.  Only the shape the fused epilogue serves is
+ * accepted: rot_dims == 96 (head_dim 128), an even head count (N % 256 == 0)
+ * and a GPU with at least two SMs; any other valid parameters return
+ * H3LIN_E_UNSUPPORTED (use the two calls above).  Errors: as h3lin_forward,
+ * plus those of h3lin_qk_norm_rope's parameters; nothing is enqueued on
+ * error.  M == 0: no-op.  Allocates nothing.
+ *
+ * h3lin_forward_gemm_qk_rope is its GEMM stage alone, after
+ * h3lin_forward_prepare or h3lin_forward_prepare_produced on the same
+ * workspace (as h3lin_forward_gemm). */
+size_t       h3lin_forward_qk_rope_workspace_bytes(int64_t M, int64_t K, int64_t N, int32_t max_rank);
+h3lin_status h3lin_forward_qk_rope(const void* x, int64_t M, const float* pre_quant_scale,
+                                   const h3lin_weight* weight, const h3lin_adapter* adapter, float strength,
+                                   const h3lin_rope_params* params, const float* q_gain, const float* k_gain,
+                                   const int32_t* positions, void* out, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+h3lin_status h3lin_forward_gemm_qk_rope(int64_t M, const h3lin_weight* weight, const h3lin_adapter* adapter,
+                                        float strength, const h3lin_rope_params* params, const float* q_gain,
+                                        const float* k_gain, const int32_t* positions, void* out,
+                                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------- failure self-test */
 /* Exercises the kernels' failure path on the device without any fault: a
  * kernel waits, with a bound of `wait_cycles` SM clock cycles (1 .. 2^31), on

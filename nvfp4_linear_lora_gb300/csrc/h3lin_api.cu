@@ -131,6 +131,21 @@ bool make_out_map(CUtensorMap* m, void* base, bool f32, int64_t cols, int64_t ro
   return r == CUDA_SUCCESS;
 }
 
+// bf16 output [rows, cols] in boxes of 16 rows x 16 columns (32 bytes) with
+// the 32-byte swizzle: the fused RoPE epilogue's stores.
+bool make_out16_map(CUtensorMap* m, void* base, int64_t cols, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {uint64_t(cols), uint64_t(rows)};
+  cuuint64_t strides[1] = {uint64_t(cols) * 2};
+  cuuint32_t box[2] = {16, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major 2-D tensor [rows, inner] with a 128-byte-swizzled box.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
@@ -215,6 +230,26 @@ struct Producer {
   uint8_t* ws;        // the consumer's workspace
 };
 
+// The parameter rules of h3lin_qk_norm_rope (shared with the fused form).
+h3lin_status validate_rope_params(const h3lin_rope_params* p) {
+  if (!p) return H3LIN_E_INVALID;
+  if (!std::isfinite(p->theta) || !(p->theta > 0.0f) || !std::isfinite(p->eps) || p->eps < 0.0f)
+    return H3LIN_E_INVALID;
+  if (p->heads < 1 || p->head_dim != 128 || p->rot_dims < 16 || p->rot_dims > p->head_dim ||
+      p->rot_dims % 16 != 0 || int64_t(p->heads) * 3 * p->head_dim > kMaxDim)
+    return H3LIN_E_SHAPE;
+  int64_t sum = 0;
+  for (int a = 0; a < 3; ++a) {
+    if (p->axis_dims[a] < 0 || p->axis_dims[a] % 2 != 0) return H3LIN_E_SHAPE;
+    sum += p->axis_dims[a];
+  }
+  return sum == p->rot_dims ? H3LIN_OK : H3LIN_E_SHAPE;
+}
+
+size_t rope_table_bytes(int64_t M) {
+  return align_up(size_t((M + 15) / 16 * 16) * kRopePairs * sizeof(float2), kRegionAlign);
+}
+
 // Host-side validation shared by h3lin_forward and its two stages.  `need_x`
 // / `need_out` say which side of the call is being checked.
 h3lin_status validate_forward(const void* x, int64_t M, const float* pqs, const h3lin_weight* w, int32_t epilogue,
@@ -267,6 +302,31 @@ h3lin_status validate_forward(const void* x, int64_t M, const float* pqs, const 
   return H3LIN_OK;
 }
 
+// Every check of h3lin_forward_qk_rope and its GEMM stage (bf16 output, no
+// SiLU*up), so that nothing is enqueued on error.
+h3lin_status validate_qk_rope(const void* x, int64_t M, const float* pqs, const h3lin_weight* w,
+                              const h3lin_adapter* adapter, float strength, const h3lin_rope_params* p,
+                              const float* q_gain, const float* k_gain, const int32_t* positions, void* out,
+                              void* ws, size_t ws_bytes, bool need_x, ForwardCall* c) {
+  h3lin_status s = validate_rope_params(p);
+  if (s != H3LIN_OK) return s;
+  if (p->rot_dims != 2 * kRopePairs) return H3LIN_E_UNSUPPORTED;
+  if (!w) return H3LIN_E_INVALID;
+  if (w->N != int64_t(3) * p->heads * p->head_dim) return H3LIN_E_SHAPE;
+  if (w->N % 256 != 0) return H3LIN_E_UNSUPPORTED;   // an odd head count: no CTA-pair tiles
+  if (M > 0) {
+    if (!q_gain || !k_gain || !positions) return H3LIN_E_INVALID;
+    if (!aligned16(q_gain) || !aligned16(k_gain) || (reinterpret_cast<uintptr_t>(positions) & 3u))
+      return H3LIN_E_ALIGN;
+  }
+  // the angle table follows h3lin_forward's regions: those must fit in the rest
+  const size_t table = M > 0 && M <= kMaxDim ? rope_table_bytes(M) : 0;
+  s = validate_forward(x, M, pqs, w, H3LIN_EPI_NONE, adapter, strength, out, H3LIN_OUT_BF16, ws,
+                       ws_bytes >= table ? ws_bytes - table : 0, need_x, true, c);
+  if (s != H3LIN_OK || c->M == 0) return s;
+  return c->dev.sm_count >= 2 ? H3LIN_OK : H3LIN_E_UNSUPPORTED;
+}
+
 // amax pass (fused with u = A(x) when the adapter is active) + quantise pass.
 // With c.produced the amax pass is skipped: the partials (and their count)
 // were left in the workspace header by the producer GEMM of x.
@@ -315,7 +375,16 @@ h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
 // producer (bf16 output only) the amax of the output for the consuming
 // projection is left in the producer's workspace: from the pair kernel's
 // SiLU*up epilogue, else by an amax pass over the output.
-h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream, const Producer* prod = nullptr) {
+// The fused Q/K RMSNorm + RoPE epilogue's inputs (h3lin_forward_qk_rope).
+struct RopeCall {
+  const h3lin_rope_params* p;
+  const float* q_gain;
+  const float* k_gain;
+  const int32_t* positions;
+};
+
+h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream, const Producer* prod = nullptr,
+                          const RopeCall* rope = nullptr) {
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
   void* xq = c.ws + c.L.codes;
@@ -351,6 +420,16 @@ h3lin_status enqueue_gemm(const ForwardCall& c, cudaStream_t stream, const Produ
            make_sf_map(&g.tm_ws, g.ws, size_t(c.N) * size_t(c.K / 16)) &&
            make_out_map(&g.tm_out, c.out, c.f32out, g.ldo, c.M);
   g.group_m = raster_group(c.N, c.K, g.pair ? 256 : 128);
+  if (rope) {   // after the (cos, sin) table: the pair kernel's epilogue normalises and rotates Q and K
+    if (!g.pair) return H3LIN_E_UNSUPPORTED;
+    if (!make_out16_map(&g.tm_out16, c.out, g.ldo, c.M)) return H3LIN_E_CUDA;
+    float4* cs = reinterpret_cast<float4*>(c.ws + c.L.total);
+    const int axis[3] = {rope->p->axis_dims[0], rope->p->axis_dims[1], rope->p->axis_dims[2]};
+    if (launch_rope_table(cs, int(c.M), axis, rope->p->theta, rope->positions, g.status, c.dev.sm_count,
+                          stream) != cudaSuccess)
+      return H3LIN_E_CUDA;
+    g.rope = RopeEpi{cs, rope->q_gain, rope->k_gain, rope->p->heads, rope->p->eps};
+  }
   const bool fused_amax = prod && g.pair && c.silu && !c.f32out;
   if (fused_amax) {
     g.amax_s = prod->pqs;
@@ -501,6 +580,36 @@ h3lin_status h3lin_forward_prepare_produced(const void* x, int64_t M, const floa
   return enqueue_prepare(c, stream);
 }
 
+size_t h3lin_forward_qk_rope_workspace_bytes(int64_t M, int64_t K, int64_t N, int32_t max_rank) {
+  if (M < 0 || K < 64 || K % 64 != 0 || N < 1 || max_rank < 0) return 0;
+  return forward_layout(M, K, N, max_rank).total + rope_table_bytes(M);
+}
+
+h3lin_status h3lin_forward_gemm_qk_rope(int64_t M, const h3lin_weight* w, const h3lin_adapter* adapter,
+                                        float strength, const h3lin_rope_params* p, const float* q_gain,
+                                        const float* k_gain, const int32_t* positions, void* out, void* ws,
+                                        size_t ws_bytes, cudaStream_t stream) {
+  ForwardCall c;
+  const h3lin_status s = validate_qk_rope(nullptr, M, nullptr, w, adapter, strength, p, q_gain, k_gain, positions,
+                                          out, ws, ws_bytes, false, &c);
+  if (s != H3LIN_OK || c.M == 0) return s;
+  const RopeCall rc{p, q_gain, k_gain, positions};
+  return enqueue_gemm(c, stream, nullptr, &rc);
+}
+
+h3lin_status h3lin_forward_qk_rope(const void* x, int64_t M, const float* pqs, const h3lin_weight* w,
+                                   const h3lin_adapter* adapter, float strength, const h3lin_rope_params* p,
+                                   const float* q_gain, const float* k_gain, const int32_t* positions, void* out,
+                                   void* ws, size_t ws_bytes, cudaStream_t stream) {
+  ForwardCall c;
+  h3lin_status s = validate_qk_rope(x, M, pqs, w, adapter, strength, p, q_gain, k_gain, positions, out, ws, ws_bytes,
+                                    true, &c);
+  if (s != H3LIN_OK || c.M == 0) return s;
+  if ((s = enqueue_prepare(c, stream)) != H3LIN_OK) return s;
+  const RopeCall rc{p, q_gain, k_gain, positions};
+  return enqueue_gemm(c, stream, nullptr, &rc);
+}
+
 size_t h3lin_mlp_workspace_bytes(int64_t M, int64_t K, int64_t N_gate_up, int64_t N_down, int32_t max_rank) {
   if (M < 0 || K < 64 || K % 64 != 0 || N_gate_up < 256 || N_gate_up % 256 != 0 || N_down < 1 || max_rank < 0)
     return 0;
@@ -555,18 +664,9 @@ h3lin_status h3lin_read_status(const void* ws, cudaStream_t stream, int32_t* dev
 extern "C" h3lin_status h3lin_qk_norm_rope(void* qkv, int64_t M, const h3lin_rope_params* p, const float* q_gain,
                                            const float* k_gain, const int32_t* positions, void* ws,
                                            size_t ws_bytes, cudaStream_t stream) {
-  if (!p) return H3LIN_E_INVALID;
-  if (!std::isfinite(p->theta) || !(p->theta > 0.0f) || !std::isfinite(p->eps) || p->eps < 0.0f)
-    return H3LIN_E_INVALID;
-  if (M < 0 || M > kMaxDim || p->heads < 1 || p->head_dim != 128 || p->rot_dims < 16 ||
-      p->rot_dims > p->head_dim || p->rot_dims % 16 != 0 || int64_t(p->heads) * 3 * p->head_dim > kMaxDim)
-    return H3LIN_E_SHAPE;
-  int64_t sum = 0;
-  for (int a = 0; a < 3; ++a) {
-    if (p->axis_dims[a] < 0 || p->axis_dims[a] % 2 != 0) return H3LIN_E_SHAPE;
-    sum += p->axis_dims[a];
-  }
-  if (sum != p->rot_dims) return H3LIN_E_SHAPE;
+  const h3lin_status v = validate_rope_params(p);
+  if (v != H3LIN_OK) return v;
+  if (M < 0 || M > kMaxDim) return H3LIN_E_SHAPE;
   if (M == 0) return H3LIN_OK;
   if (!qkv || !q_gain || !k_gain || !positions || !ws) return H3LIN_E_INVALID;
   if (!aligned16(qkv) || !aligned16(q_gain) || !aligned16(k_gain) || !aligned16(ws) ||

@@ -370,11 +370,13 @@ struct PairCfg {
   static constexpr int kSfCols = 16 + 32;
   static constexpr int kEpiWarps = 16;
   static constexpr int kEpiScratch = 2048;                                          // 32 rows x 64 bytes
+  static constexpr int kRopeGainBytes = 1024;                                      // fused RoPE: Q, K gains
   static constexpr int kSmem = kStages * kStageBytes + kEpiWarps * kEpiScratch + 1024 + 512;
+  static constexpr int kSmemRope = kSmem + kRopeGainBytes;
   static constexpr int kTmemCols = 512;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(256 + kStages * kSfCols <= kTmemCols, "TMEM budget");
-  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kSmemRope <= 232448, "shared memory budget");
 };
 
 // silu(g) * u with g = scale * acc_gate, u = scale * acc_up (fast exp and divide;
@@ -453,29 +455,174 @@ __device__ __forceinline__ void epi_scratch_ready(int lane) {
   __syncwarp();
 }
 
+// Fused Q/K RMSNorm + split-half RoPE: one warp's part of a Q or K tile, one
+// head (the 128 accumulator columns at tq's column) x 16 rows (the 16 TMEM
+// lanes at tq's lane), bf16 output.  With the 16-lane x 2 TMEM load shape lane l holds row
+// l % 16 and, by half h = l / 16, 64 of the head's dimensions in three runs
+// ("slots"):
+//   slots  0..31   h = 0: dims 16..47    h = 1: dims 64..95
+//   slots 32..47   h = 0: dims  0..15    h = 1: dims 96..111
+//   slots 48..63   h = 0: dims 48..63    h = 1: dims 112..127
+// The rotation partner (d +- 48) of slot s < 32 is slot s of lane l ^ 16; on
+// h = 0 slots 32 + k and 48 + k are each other's partners; h = 1's slots from
+// 32 on are not rotated.  Every value is the float k_qk_norm_rope computes
+// from the stored bf16 output: the same bf16 rounding of the scaled
+// accumulator, the sum of squares as the same tree (8-dimension fma chains,
+// then chunks 8, 4, 2 and 1 apart; the other half's chunks one shuffle away),
+// the same normalisation and rotation expressions.  Stores: slots 0..31 go
+// straight to global memory (16 bytes a lane), slots 32..63 through the
+// warp's staging block as four 16-row x 16-column TMA boxes (tm16).
+__device__ __forceinline__ void rope_head_epilogue(uint32_t tq, uint32_t leader_tmem_empty, float scale, float post,
+                                                   const float* gain, const float4* __restrict__ cs, int row, int M,
+                                                   __nv_bfloat16* __restrict__ out, int col0, int ldo, float eps,
+                                                   int lane, uint32_t* status, uint8_t* scratch,
+                                                   const CUtensorMap* tm16, int row0) {
+  const int h = lane >> 4;
+  epi_scratch_ready(lane);   // a V tile's TMA store may still be reading the staging block
+  uint32_t v[32];   // the bf16 output values, slot order, two per word
+  float sm[8];      // sums of squares of the 8-dimension slot chunks
+  {
+    uint32_t a[32], b[16], c[16];
+    tmem_ld16x2_x32<48>(tq + 16, a);   // slots 0..31
+    tmem_ld16x2_x16<96>(tq + 0, b);    // slots 32..47
+    tmem_ld16x2_x16<64>(tq + 48, c);   // slots 48..63
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const uint32_t lo = k < 16 ? a[2 * k] : (k < 24 ? b[2 * k - 32] : c[2 * k - 48]);
+      const uint32_t hi = k < 16 ? a[2 * k + 1] : (k < 24 ? b[2 * k - 31] : c[2 * k - 47]);
+      float ylo, yhi;
+      fmul2_rn(__uint_as_float(lo), __uint_as_float(hi), scale, scale, ylo, yhi);
+      fmul2_rn(ylo, yhi, post, post, ylo, yhi);   // post = 1 but for tiny tensor scales: exact then
+      v[k] = pack_bf16x2(ylo, yhi);
+      float ss = (k & 3) ? sm[k >> 2] : 0.0f;
+      ss = fmaf(bf16lo(v[k]), bf16lo(v[k]), ss);
+      sm[k >> 2] = fmaf(bf16hi(v[k]), bf16hi(v[k]), ss);
+    }
+  }
+  // the sum of squares over the head: the tree over its 16 chunks in
+  // dimension order (h = 0 holds chunks 0..7 in slot-chunk order 2 3 4 5 0 1
+  // 6 7, h = 1 chunks 8..15 in order), each add's operands the same floats
+  constexpr int kChunkOfSlot0[8] = {4, 5, 0, 1, 2, 3, 6, 7};   // h = 0: slot chunk holding dimension chunk j
+  float t1[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float g = h ? sm[j] : sm[kChunkOfSlot0[j]];
+    t1[j] = g + __shfl_xor_sync(0xFFFFFFFFu, g, 16);
+  }
+  const float ss = ((t1[0] + t1[4]) + (t1[2] + t1[6])) + ((t1[1] + t1[5]) + (t1[3] + t1[7]));
+  const float r = rsqrtf(fmaf(ss, 1.0f / 128.0f, eps));
+
+  // slots 32..63 wait in the warp's staging block (free in this path) while
+  // slots 0..31 are rotated: 16 registers fewer in flight
+  {
+    uint4* st4 = reinterpret_cast<uint4*>(scratch) + lane * 4;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      st4[c ^ ((lane >> 1) & 3)] = make_uint4(v[16 + 4 * c], v[17 + 4 * c], v[18 + 4 * c], v[19 + 4 * c]);
+  }
+  const bool live = row < M;
+  const int trow = live ? row : M - 1;   // the warp's 16 rows read one 256-byte run per float4
+  const float4* csr = cs + int64_t(trow >> 4) * (16 * kRopePairs / 2) + (trow & 15);
+  const float2* g2 = reinterpret_cast<const float2*>(gain);
+  __nv_bfloat16* orow = out + int64_t(live ? row : 0) * ldo + col0;
+  // slots 0..31: rotation with the other half's slot (angles 16..47); h = 0
+  // subtracts the partner's sine term, h = 1 adds it
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int d = h ? 64 + 8 * m : 16 + 8 * m;
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 t = __ldg(csr + 16 * (8 + 4 * m + k));   // (cos, sin) of angles 16 + 8m + 2k, + 1
+      const float2 g = g2[(d >> 1) + k];
+      const uint32_t w = v[4 * m + k];
+      const float y0 = bf16lo(w) * r * g.x, y1 = bf16hi(w) * r * g.y;
+      const float p0 = __shfl_xor_sync(0xFFFFFFFFu, y0, 16), p1 = __shfl_xor_sync(0xFFFFFFFFu, y1, 16);
+      o[k] = pack_bf16x2(fmaf(p0, h ? t.y : -t.y, y0 * t.x), fmaf(p1, h ? t.w : -t.w, y1 * t.z));
+    }
+    if (live && in_bounds(col0 + d + 8 <= ldo, status))
+      *reinterpret_cast<uint4*>(orow + d) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  {
+    const uint4* st4 = reinterpret_cast<const uint4*>(scratch) + lane * 4;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 w4 = st4[c ^ ((lane >> 1) & 3)];
+      v[16 + 4 * c] = w4.x;
+      v[17 + 4 * c] = w4.y;
+      v[18 + 4 * c] = w4.z;
+      v[19 + 4 * c] = w4.w;
+    }
+  }
+  __syncwarp();   // every lane has its slots back before the block holds outputs
+  // slots 32..63: h = 0 rotates dims j and j + 48 (angles 0..15) with each
+  // other; h = 1's dims 96..127 keep y (cos 1, sin +0, partner itself)
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int da = h ? 96 + 8 * m : 8 * m, db = h ? 112 + 8 * m : 48 + 8 * m;
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 t = h ? make_float4(1.0f, 0.0f, 1.0f, 0.0f) : __ldg(csr + 16 * (4 * m + k));
+      const float2 ga = g2[(da >> 1) + k], gb = g2[(db >> 1) + k];
+      const uint32_t wa = v[16 + 4 * m + k], wb = v[24 + 4 * m + k];
+      const float ya0 = bf16lo(wa) * r * ga.x, ya1 = bf16hi(wa) * r * ga.y;
+      const float yb0 = bf16lo(wb) * r * gb.x, yb1 = bf16hi(wb) * r * gb.y;
+      oa[k] = pack_bf16x2(fmaf(h ? ya0 : yb0, h ? 0.0f : -t.y, ya0 * t.x),
+                          fmaf(h ? ya1 : yb1, h ? 0.0f : -t.w, ya1 * t.z));
+      ob[k] = pack_bf16x2(fmaf(h ? yb0 : ya0, h ? 0.0f : t.y, yb0 * t.x),
+                          fmaf(h ? yb1 : ya1, h ? 0.0f : t.w, yb1 * t.z));
+    }
+    // boxes of 16 rows x 32 bytes (a: dims 0.. or 96.., b: 48.. or 112..), 32-byte swizzle
+    const int rr = lane & 15;
+    const int sw = (m ^ ((rr >> 2) & 1)) << 4;
+    *reinterpret_cast<uint4*>(scratch + (h ? 2 : 0) * 512 + rr * 32 + sw) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *reinterpret_cast<uint4*>(scratch + (h ? 3 : 1) * 512 + rr * 32 + sw) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm16, scratch, col0 + 0, row0);
+    tma_store_2d(tm16, scratch + 512, col0 + 48, row0);
+    tma_store_2d(tm16, scratch + 1024, col0 + 96, row0);
+    tma_store_2d(tm16, scratch + 1536, col0 + 112, row0);
+    bulk_commit_group();
+  }
+}
+
 // AMAX (SiLU*up with a bf16 output only): the epilogue also reduces
 // max |float(h) * s_next| over the tile's valid rows, h the bf16 value it
 // stores and s_next the per-channel pre_quant_scale of the projection that
 // consumes h (null = 1); each CTA writes its maximum to amax_out[blockIdx.x]
 // and CTA 0 the count gridDim.x to *amax_count.  The consumer's quantiser
 // then needs no amax pass over h.
-template <bool SILU, bool LORA, bool F32OUT, bool AMAX>
+//
+// ROPE (bf16 output of a fused QKV projection without SiLU*up): the tiles of
+// Q and K heads take rope_head_epilogue; V tiles are stored as usual.
+template <bool SILU, bool LORA, bool F32OUT, bool AMAX, bool ROPE>
 __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_wq,
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_b,
     const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_ws,
-    const __grid_constant__ CUtensorMap tm_out,
+    const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_out16,
     const float* __restrict__ ts_x, const float* __restrict__ ts_w, void* __restrict__ out, int M, int N, int K,
     int rank, int ldo, int group_m, uint32_t* __restrict__ status, const float* __restrict__ amax_s,
-    float* __restrict__ amax_out, int* __restrict__ amax_count) {
+    float* __restrict__ amax_out, int* __restrict__ amax_count, const RopeEpi rope) {
   static_assert(!AMAX || (SILU && !F32OUT), "the fused amax serves the bf16 SiLU*up output");
+  static_assert(!ROPE || (!SILU && !F32OUT && !AMAX), "the fused RoPE serves the bf16 QKV output");
   using C = PairCfg;
   constexpr int kPairCpWarps = PairRoles<SILU>::kCpWarps;
   constexpr int kPairEpiWarp0 = PairRoles<SILU>::kEpiWarp0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi_scratch = smem + C::kStages * C::kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(epi_scratch + C::kEpiWarps * C::kEpiScratch);
+  float* rope_gain = reinterpret_cast<float*>(epi_scratch + C::kEpiWarps * C::kEpiScratch);   // ROPE: Q, K gains
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_scratch + C::kEpiWarps * C::kEpiScratch +
+                                               (ROPE ? C::kRopeGainBytes : 0));
   uint64_t* empty = full + C::kStages;
   uint64_t* sf_full = empty + C::kStages;
   uint64_t* tmem_full = sf_full + C::kStages;
@@ -516,6 +663,8 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
     tmem_alloc_pair(tmem_slot, C::kTmemCols);
     tmem_relinquish_pair();
   }
+  if (ROPE && threadIdx.x < 256)
+    rope_gain[threadIdx.x] = threadIdx.x < 128 ? rope.q_gain[threadIdx.x] : rope.k_gain[threadIdx.x - 128];
   tc_fence_before();
   cluster_sync_all();
   tc_fence_after();
@@ -693,6 +842,17 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
       tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
       if (!mbar_wait(tmem_full, acc_ph, ab)) break;
       tc_fence_after();
+      if (ROPE && tn < rope.heads) {   // the tile's two heads are both Q or both K heads
+        const int hs = c4 >> 1, rh = c4 & 1;   // head of the tile, half of the quarter's rows
+        const int head = 2 * tn + hs;
+        rope_head_epilogue(tmem + (static_cast<uint32_t>(32 * q + 16 * rh) << 16) + 128 * hs, leader_tmem_empty,
+                           scale, *epi_post, rope_gain + (head < rope.heads ? 0 : 128), rope.cs,
+                           tm * 256 + 128 * static_cast<int>(crank) + 32 * q + 16 * rh + (lane & 15), M,
+                           static_cast<__nv_bfloat16*>(out), 128 * head, ldo, rope.eps, lane, status, scratch,
+                           &tm_out16, tm * 256 + 128 * static_cast<int>(crank) + 32 * q + 16 * rh);
+        acc_ph ^= 1;
+        continue;
+      }
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
       const int row0 = tm * 256 + 128 * static_cast<int>(crank) + 32 * q;   // first row of this warp
       const int col0 = SILU ? tn * 128 + c4 * 32 : tn * 256 + c4 * 64;
@@ -757,10 +917,11 @@ __global__ void __launch_bounds__(PairRoles<SILU>::kThreads, 1) k_fp4gemm_pair(
   }
 }
 
-template <bool SILU, bool LORA, bool F32OUT, bool AMAX = false>
+template <bool SILU, bool LORA, bool F32OUT, bool AMAX = false, bool ROPE = false>
 static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStream_t st) {
-  auto kern = k_fp4gemm_pair<SILU, LORA, F32OUT, AMAX>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
+  auto kern = k_fp4gemm_pair<SILU, LORA, F32OUT, AMAX, ROPE>;
+  const int smem = ROPE ? PairCfg::kSmemRope : PairCfg::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles_m = (a.M + 255) / 256;
   const int tiles_n = SILU ? (a.N / 2) / 128 : a.N / 256;
@@ -770,7 +931,7 @@ static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStre
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(PairRoles<SILU>::kThreads);
-  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -779,16 +940,21 @@ static cudaError_t launch_pair_variant(const GemmArgs& a, int sm_count, cudaStre
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  trace_launch("k_fp4gemm_pair", grid, 2, PairRoles<SILU>::kThreads, PairCfg::kSmem,
-               "silu=%d lora=%d f32out=%d amax=%d M=%d N=%d K=%d rank=%d tiles=%d raster_group=%d", int(SILU),
-               int(LORA), int(F32OUT), int(AMAX), a.M, a.N, a.K, a.rank, tiles, a.group_m);
-  return cudaLaunchKernelEx(&cfg, kern, a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.tm_xs, a.tm_ws, a.tm_out, a.ts_x, a.ts_w,
+  trace_launch("k_fp4gemm_pair", grid, 2, PairRoles<SILU>::kThreads, smem,
+               "silu=%d lora=%d f32out=%d amax=%d rope=%d M=%d N=%d K=%d rank=%d tiles=%d raster_group=%d",
+               int(SILU), int(LORA), int(F32OUT), int(AMAX), int(ROPE), a.M, a.N, a.K, a.rank, tiles, a.group_m);
+  return cudaLaunchKernelEx(&cfg, kern, a.tm_xq, a.tm_wq, a.tm_u, a.tm_b, a.tm_xs, a.tm_ws, a.tm_out, a.tm_out16,
+                            a.ts_x, a.ts_w,
                             a.out, a.M, a.N, a.K, a.rank, a.ldo, a.group_m, a.status, a.amax_s, a.amax_out,
-                            a.amax_count);
+                            a.amax_count, a.rope);
 }
 
 template <bool F32OUT>
 static cudaError_t launch_pair_dtype(const GemmArgs& a, int sm_count, cudaStream_t st) {
+  if (!F32OUT && !a.silu && a.rope.cs) {
+    return a.lora ? launch_pair_variant<false, true, false, false, true>(a, sm_count, st)
+                  : launch_pair_variant<false, false, false, false, true>(a, sm_count, st);
+  }
   if (!F32OUT && a.silu && a.amax_out) {
     return a.lora ? launch_pair_variant<true, true, false, true>(a, sm_count, st)
                   : launch_pair_variant<true, false, false, true>(a, sm_count, st);

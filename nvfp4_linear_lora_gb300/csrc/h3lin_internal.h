@@ -62,11 +62,25 @@ cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, 
                               void* codes, void* scales, float* ts_out, void* u, uint32_t* status,
                               const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
                               int sm_count, cudaStream_t st);
+// Q/K RMSNorm + split-half RoPE in the pair GEMM's epilogue (bf16 output of
+// a fused QKV projection, head_dim 128, 96 rotated dimensions): the tiles of
+// Q and K heads are normalised and rotated before they are stored, exactly as
+// k_qk_norm_rope would do in place afterwards; V tiles are stored as usual.
+struct RopeEpi {
+  const float4* cs;      // the rows' (cos, sin) of the 48 rotation pairs (launch_rope_table's layout)
+  const float* q_gain;   // [128]
+  const float* k_gain;   // [128]
+  int heads;             // Q heads (= K heads); the output is [Q | K | V]
+  float eps;
+};
+constexpr int kRopePairs = 48;   // rotation pairs per head in the fused epilogue
+
 // FP4 GEMM + optional LoRA-up + epilogue.
 struct GemmArgs {
   CUtensorMap tm_xq, tm_wq, tm_u, tm_b;
   CUtensorMap tm_xs, tm_ws;   // scale bytes viewed as [bytes / 256, 256] (pair kernel)
   CUtensorMap tm_out;         // output [M, ldo], 32-row x 128-byte boxes (pair kernel)
+  CUtensorMap tm_out16;       // output [M, ldo] bf16, 16-row x 16-column boxes, 32-byte swizzle (fused RoPE)
   const uint8_t* xs;
   const uint8_t* ws;
   const float* ts_x;
@@ -82,6 +96,8 @@ struct GemmArgs {
   const float* amax_s;
   float* amax_out;
   int* amax_count;
+  // fused Q/K RMSNorm + RoPE (pair kernel, no SiLU, bf16 output); rope.cs null = off
+  RopeEpi rope;
 };
 cudaError_t launch_fp4gemm(const GemmArgs& a, int sm_count, cudaStream_t st);
 
@@ -94,6 +110,12 @@ int raster_group(int64_t N, int64_t K, int tile_rows);
 cudaError_t launch_qk_norm_rope(void* qkv, int M, int heads, int rot, const int (&axis_dims)[3], float theta,
                                 float eps, const float* q_gain, const float* k_gain, const int* pos,
                                 uint32_t* status, int sm_count, cudaStream_t st);
+// The (cos, sin) table of the fused epilogue: for the 48 rotation pairs of
+// every row, the same floats k_qk_norm_rope computes, in blocks of 16 rows:
+// cs[(m / 16) * 24 * 16 + j * 16 + m % 16] = (cos, sin) of pairs 2j, 2j + 1
+// of row m; ceil(M / 16) * 16 * 384 bytes.
+cudaError_t launch_rope_table(float4* cs, int M, const int (&axis_dims)[3], float theta, const int* pos,
+                              uint32_t* status, int sm_count, cudaStream_t st);
 
 // Modulation producer (h3lin_modulate.cu): x_mod = bf16(LN(x) (1 + scale) +
 // shift) per row's table row, plus amax partials of |x_mod * pqs| and their count.

@@ -152,11 +152,36 @@ __global__ void __launch_bounds__(kRopeThreads, 2) k_qk_norm_rope(__nv_bfloat16*
   }
 }
 
-}  // namespace
+// The rotation angles' (cos, sin) for the QKV GEMM's fused epilogue, with
+// k_qk_norm_rope's angle arithmetic (float(pos) x the host-rounded frequency,
+// one rounding, then sincosf), so the fused epilogue rotates by exactly the
+// same values.  Layout: blocks of 16 rows; in a block, float4 j (pairs 2j and
+// 2j + 1: cos, sin, cos, sin) of its 16 rows side by side, so that the 16
+// rows an epilogue warp holds read one 256-byte run per float4.
+__global__ void __launch_bounds__(256) k_rope_table(float4* __restrict__ cs, int M, const int* __restrict__ pos,
+                                                    uint32_t* status, RopeFreqs f) {
+  constexpr int kQuads = kRopePairs / 2;
+  const int64_t n = (int64_t(M) + 15) / 16 * 16 * kQuads;   // whole 16-row blocks; rows >= M are skipped
+  for (int64_t t = int64_t(blockIdx.x) * 256 + threadIdx.x; t < n; t += int64_t(gridDim.x) * 256) {
+    const int64_t blk = t / (16 * kQuads);
+    const int rem = static_cast<int>(t - blk * (16 * kQuads));
+    const int j = rem >> 4;
+    const int64_t row = blk * 16 + (rem & 15);
+    if (row >= M) continue;
+    float c[2], sn[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = 2 * j + e;
+      const float a = __fmul_rn(static_cast<float>(pos[3 * row + f.axis[i]]), f.freq[i]);
+      sincosf(a, &sn[e], &c[e]);
+    }
+    if (in_bounds(t < n, status)) cs[t] = make_float4(c[0], sn[0], c[1], sn[1]);   // t = blk 384 + j 16 + row % 16
+  }
+}
 
-cudaError_t launch_qk_norm_rope(void* qkv, int M, int heads, int rot, const int (&axis_dims)[3], float theta,
-                                float eps, const float* q_gain, const float* k_gain, const int* pos,
-                                uint32_t* status, int sm_count, cudaStream_t st) {
+// Per pair i of the rot / 2 rotation pairs: theta^(-2 j / axis_dims[a]) (in
+// double, rounded once to float) and its position axis a.
+RopeFreqs rope_freqs(const int (&axis_dims)[3], float theta) {
   RopeFreqs f{};
   int i = 0;
   for (int a = 0; a < 3; ++a)
@@ -164,6 +189,27 @@ cudaError_t launch_qk_norm_rope(void* qkv, int M, int heads, int rot, const int 
       f.freq[i] = static_cast<float>(std::pow(static_cast<double>(theta), -2.0 * j / axis_dims[a]));
       f.axis[i] = a;
     }
+  return f;
+}
+
+}  // namespace
+
+cudaError_t launch_rope_table(float4* cs, int M, const int (&axis_dims)[3], float theta, const int* pos,
+                              uint32_t* status, int sm_count, cudaStream_t st) {
+  const RopeFreqs f = rope_freqs(axis_dims, theta);
+  const int64_t n = (int64_t(M) + 15) / 16 * 16 * (kRopePairs / 2);   // whole 16-row blocks (rows >= M skipped)
+  int64_t grid = (n + 255) / 256;
+  if (grid > int64_t(8) * sm_count) grid = int64_t(8) * sm_count;
+  if (grid < 1) grid = 1;
+  trace_launch("k_rope_table", grid, 1, 256, 0, "M=%d pairs=%d", M, kRopePairs);
+  k_rope_table<<<static_cast<unsigned>(grid), 256, 0, st>>>(cs, M, pos, status, f);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qk_norm_rope(void* qkv, int M, int heads, int rot, const int (&axis_dims)[3], float theta,
+                                float eps, const float* q_gain, const float* k_gain, const int* pos,
+                                uint32_t* status, int sm_count, cudaStream_t st) {
+  const RopeFreqs f = rope_freqs(axis_dims, theta);
   const int row_bytes = heads * 512;
   const int fixed = 128 + 256 * 4 + 64;                          // alignment, gains, flag
   const int per_stage = row_bytes + 2 * kRopeMaxPairs * 4 + 16;  // data, angles, two barriers

@@ -91,6 +91,11 @@ _SIGNATURES = {
                                  _vp, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter), _f32,
                                  _vp, _vp, _i32, _vp, _sz, _vp]),
     "h3lin_qk_norm_rope": (_i32, [_vp, _i64, ctypes.POINTER(h3lin_rope_params), _vp, _vp, _vp, _vp, _sz, _vp]),
+    "h3lin_forward_qk_rope_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
+    "h3lin_forward_qk_rope": (_i32, [_vp, _i64, _vp, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter),
+                                     _f32, ctypes.POINTER(h3lin_rope_params), _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "h3lin_forward_gemm_qk_rope": (_i32, [_i64, ctypes.POINTER(h3lin_weight), ctypes.POINTER(h3lin_adapter), _f32,
+                                          ctypes.POINTER(h3lin_rope_params), _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_modulate_produce": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp]),
     "h3lin_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "h3lin_selftest_wait_timeout": (_i32, [_vp, _sz, _i64, _vp]),
@@ -211,6 +216,22 @@ def h3lin_mlp_forward(x, M, gu_pqs, gate_up, gu_adapter, gu_strength, down_pqs, 
 
 def h3lin_qk_norm_rope(qkv, M, params, q_gain, k_gain, positions, ws, ws_bytes, stream):
     return lib().h3lin_qk_norm_rope(qkv, M, _ref(params), q_gain, k_gain, positions, ws, ws_bytes, stream)
+
+
+def h3lin_forward_qk_rope_workspace_bytes(M, K, N, max_rank):
+    return lib().h3lin_forward_qk_rope_workspace_bytes(M, K, N, max_rank)
+
+
+def h3lin_forward_qk_rope(x, M, pqs, weight, adapter, strength, params, q_gain, k_gain, positions, out, ws, ws_bytes,
+                          stream):
+    return lib().h3lin_forward_qk_rope(x, M, pqs, _ref(weight), _ref(adapter), strength, _ref(params), q_gain,
+                                       k_gain, positions, out, ws, ws_bytes, stream)
+
+
+def h3lin_forward_gemm_qk_rope(M, weight, adapter, strength, params, q_gain, k_gain, positions, out, ws, ws_bytes,
+                               stream):
+    return lib().h3lin_forward_gemm_qk_rope(M, _ref(weight), _ref(adapter), strength, _ref(params), q_gain, k_gain,
+                                            positions, out, ws, ws_bytes, stream)
 
 
 def h3lin_modulate_produce(x, M, K, table, table_rows, row_table, eps, x_mod, next_pqs, next_ws, next_ws_bytes,
@@ -459,6 +480,30 @@ def qk_norm_rope(qkv, q_gain, k_gain, positions, heads, rot_dims=96, axis_dims=(
     _check(h3lin_qk_norm_rope(qkv.data_ptr(), qkv.shape[0], p, q_gain.data_ptr(), k_gain.data_ptr(),
                               positions.data_ptr(), ws.data_ptr(), ws.numel(), _stream()), "h3lin_qk_norm_rope")
     return qkv
+
+
+def forward_qk_rope(x, weight, q_gain, k_gain, positions, heads, pre_quant_scale=None, adapter=None, strength=1.0,
+                    rot_dims=96, axis_dims=(32, 32, 32), theta=10000.0, eps=1e-6, out=None, workspace=None):
+    """The QKV projection with Q/K RMSNorm + split-half RoPE in its epilogue
+    (``h3lin_forward_qk_rope``): the same bf16 [M, 3 * heads * 128] as
+    ``forward`` followed by ``qk_norm_rope``, in one GEMM."""
+    torch = _torch()
+    M = x.shape[0]
+    if positions.dtype != torch.int32:
+        raise TypeError("positions must be int32 [M, 3]")
+    if out is None:
+        out = _alloc((M, weight.N), torch.bfloat16, x.device)
+    if out.dtype != torch.bfloat16:
+        raise TypeError("out must be bfloat16")
+    if workspace is None:
+        workspace = new_workspace(h3lin_forward_qk_rope_workspace_bytes(M, weight.K, weight.N,
+                                                                        adapter.rank if adapter else 0), x.device)
+    p = rope_params(heads, 128, rot_dims, axis_dims, theta, eps)
+    _check(h3lin_forward_qk_rope(x.data_ptr(), M, _ptr(pre_quant_scale), weight.c_struct(),
+                                 adapter.c_struct() if adapter is not None else None, float(strength), p,
+                                 q_gain.data_ptr(), k_gain.data_ptr(), positions.data_ptr(), out.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(), _stream()), "h3lin_forward_qk_rope")
+    return out
 
 
 def modulate_produce(x, table, row_table, next_workspace, next_pre_quant_scale=None, eps=1e-6, out=None):

@@ -230,6 +230,49 @@ def test_qk_norm_rope_argument_checks():
     assert call(ws_bytes=64) == E.H3LIN_E_WORKSPACE
 
 
+def test_forward_qk_rope_argument_checks():
+    E = h3lin
+    w = _weight(3 * 4 * 128, 256)   # 4 heads
+
+    def full(M=10, x=A, w=w, qg=A, kg=A, pos=A, out=A, ws=A, ws_bytes=1 << 30, **kw):
+        prm = dict(heads=4, head_dim=128, rot_dims=96, axis_dims=(32, 32, 32), theta=10000.0, eps=1e-6)
+        prm.update(kw)
+        return h3lin.h3lin_forward_qk_rope(x, M, None, w, None, 1.0, h3lin.rope_params(**prm), qg, kg, pos, out,
+                                           ws, ws_bytes, None)
+
+    def gemm(M=10, w=w, qg=A, kg=A, pos=A, out=A, ws=A, ws_bytes=1 << 30, **kw):
+        prm = dict(heads=4, head_dim=128, rot_dims=96, axis_dims=(32, 32, 32), theta=10000.0, eps=1e-6)
+        prm.update(kw)
+        return h3lin.h3lin_forward_gemm_qk_rope(M, w, None, 1.0, h3lin.rope_params(**prm), qg, kg, pos, out, ws,
+                                                ws_bytes, None)
+
+    for call in (full, gemm):
+        assert call(head_dim=64) == E.H3LIN_E_SHAPE
+        assert call(axis_dims=(32, 32, 30)) == E.H3LIN_E_SHAPE
+        assert call(theta=-1.0) == E.H3LIN_E_INVALID
+        # valid parameters the fused epilogue does not serve
+        assert call(rot_dims=64, axis_dims=(32, 16, 16)) == E.H3LIN_E_UNSUPPORTED
+        assert call(heads=3, w=_weight(3 * 3 * 128, 256)) == E.H3LIN_E_UNSUPPORTED   # N % 256 != 0
+        assert call(heads=5) == E.H3LIN_E_SHAPE                                     # N != 3 heads 128
+        assert call(w=None) == E.H3LIN_E_INVALID
+        assert call(M=-1) == E.H3LIN_E_SHAPE
+        assert call(M=0, qg=None, kg=None, pos=None, out=None, ws=None) == E.H3LIN_OK
+        assert call(qg=None) == E.H3LIN_E_INVALID
+        assert call(pos=None) == E.H3LIN_E_INVALID
+        assert call(kg=A + 4) == E.H3LIN_E_ALIGN
+        assert call(pos=A + 2) == E.H3LIN_E_ALIGN
+        assert call(out=None) == E.H3LIN_E_INVALID
+        assert call(ws=A + 8) == E.H3LIN_E_ALIGN
+    assert full(x=None) == E.H3LIN_E_INVALID
+    # the workspace must hold h3lin_forward's regions plus M * 384 bytes of angles
+    M, K, N = 1000, 256, 1536
+    need = h3lin.h3lin_forward_qk_rope_workspace_bytes(M, K, N, 0)
+    assert need >= h3lin.h3lin_forward_workspace_bytes(M, K, N, 0) + M * 48 * 8
+    assert full(M=M, ws_bytes=need - 1) == E.H3LIN_E_WORKSPACE
+    assert gemm(M=M, ws_bytes=need - 1) == E.H3LIN_E_WORKSPACE
+    assert h3lin.h3lin_forward_qk_rope_workspace_bytes(-1, K, N, 0) == 0
+
+
 def test_modulate_produce_argument_checks():
     E = h3lin
 
