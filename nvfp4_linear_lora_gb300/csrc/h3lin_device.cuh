@@ -313,6 +313,17 @@ __device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1,
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// (r0, r1) = (fma(a0, b0, c0), fma(a1, b1, c1)), each rounded once to
+// nearest even: one packed f32x2 fma (the same results as two fmaf).
+__device__ __forceinline__ void ffma2_rn(float a0, float a1, float b0, float b1, float c0, float c1, float& r0,
+                                         float& r1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // ------------------------------------------- LoRA operand and epilogue scales
 // The GEMM accumulates the base products and u.B' in one FP32 tile and
 // multiplies the sum by ts_x * ts_w in its epilogue, so B' = B * c with
