@@ -32,13 +32,22 @@ from nvfp4_linear_lora_gb300 import configs, synth  # noqa: E402
 
 
 # DRAM traffic of the GEMM launches (dram__bytes_read.sum + dram__bytes_write.sum
-# per launch) from one ncu capture of the S=37726 block, summarised in
-# profiles/dram_fp4gemm_pair_S37726.md.  It is reported only while the GEMM
-# sources hash to the value the capture was taken with; after any change to
-# them the counters no longer describe the kernel and `traffic` is null.
-GEMM_TRAFFIC = {"sources_sha256": "81cd8c5729a09808481d11bba2a1b1abcf6cc88fa163e8dbbc11e1ad7ce9306b", "S": 37726,
-                "bytes_per_launch": {"qkv": 501951488 + 1118704128, "attn_out": 134770176 + 338481920,
-                                     "gate_up": 558524672 + 1007130624, "down": 548595712 + 367817984}}
+# per launch) of the block, from one ncu capture at S=16384 (the timed step's
+# four launches; a capture at full size would exceed the size rule for a
+# multi-pass capture) scaled by the rows, 37726 / 16384: every term of a
+# launch's traffic (x panels, output, the weight once per raster group) grows
+# with M.  Summarised in profiles/dram_fp4gemm_pair_S16384.md.  It is reported
+# only while the GEMM sources hash to the value the capture was taken with;
+# after any change to them the counters no longer describe the kernel and
+# `traffic` is null.
+GEMM_TRAFFIC = {"sources_sha256": "0a254c438c5c3a314eef515553d32f6e101c71e812e6331230b39a502417cbd7", "S": 37726,
+                "scaled_from": {"S": 16384, "bytes_per_launch": {"qkv": 217108480 + 468796160,
+                                                                 "attn_out": 67608576 + 119828480,
+                                                                 "gate_up": 232174592 + 419132928,
+                                                                 "down": 252185600 + 148391680}},
+                "bytes_per_launch": {k: round(v * 37726 / 16384) for k, v in
+                                     {"qkv": 217108480 + 468796160, "attn_out": 67608576 + 119828480,
+                                      "gate_up": 232174592 + 419132928, "down": 252185600 + 148391680}.items()}}
 GEMM_SOURCES = ("nvfp4_linear_lora_gb300/csrc/h3lin_gemm.cu", "nvfp4_linear_lora_gb300/csrc/h3lin_device.cuh")
 
 
