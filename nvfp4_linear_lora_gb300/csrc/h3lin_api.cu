@@ -344,18 +344,19 @@ h3lin_status enqueue_prepare(const ForwardCall& c, cudaStream_t stream) {
   const float lora_k = c.lora ? c.strength * (c.adapter->alpha / float(c.rank)) : 0.0f;
   if (c.lora) {
     CUtensorMap tm_x, tm_a;
-    const int a_box = c.rank <= 256 ? int(c.rank) : int(c.rank / 2);
+    const int parts = lora_rank_parts(c.M, int(c.rank), c.dev.sm_count);
+    const int a_box = lora_a_box_rows(int(c.rank), parts);
     if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, c.K, c.M, c.K * 2, 64, 128)) return H3LIN_E_CUDA;
     if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.adapter->A, c.K, c.rank, c.K * 2, 64, a_box))
       return H3LIN_E_CUDA;
     if (c.produced) {   // one pass: quantise + u = A(x) + B'
-      if (launch_quant_lora(tm_x, tm_a, int(c.M), int(c.K), int(c.rank), a_box, c.pqs, partials, produced_count,
-                            xq, xs, ts_x, u, status, c.adapter->B, bp, c.N * c.rank, lora_k, c.w->tensor_scale,
-                            c.dev.sm_count, stream) != cudaSuccess)
+      if (launch_quant_lora(tm_x, tm_a, int(c.M), int(c.K), int(c.rank), parts, a_box, c.pqs, partials,
+                            produced_count, xq, xs, ts_x, u, status, c.adapter->B, bp, c.N * c.rank, lora_k,
+                            c.w->tensor_scale, c.dev.sm_count, stream) != cudaSuccess)
         return H3LIN_E_CUDA;
       return H3LIN_OK;
     }
-    if (launch_amax_lora(tm_x, tm_a, int(c.M), int(c.K), int(c.rank), a_box, c.pqs, partials, u, status,
+    if (launch_amax_lora(tm_x, tm_a, int(c.M), int(c.K), int(c.rank), parts, a_box, c.pqs, partials, u, status,
                          c.dev.sm_count, &nparts, stream) != cudaSuccess)
       return H3LIN_E_CUDA;
   } else if (!c.produced) {

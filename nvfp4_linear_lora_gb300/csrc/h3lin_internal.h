@@ -50,14 +50,18 @@ cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const fl
                          // written by the amax pass) takes a power of two from B' for tiny tensor scales
                          const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
                          void* u, int64_t u_elems, uint32_t* status, int sm_count, cudaStream_t st);
+// Rank parts of the LoRA-down passes for M rows (1 at full size) and the
+// matching box rows of A's tensor map (h3lin_quant.cu).
+int lora_rank_parts(int64_t M, int rank, int sm_count);
+int lora_a_box_rows(int rank, int parts);
 // amax pass fused with u = A(x) (bf16 [M, rank]); returns grid size in *nparts.
-cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank, int parts,
                              int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
                              int sm_count, int* nparts, cudaStream_t st);
 // The same TMA-staged pass with the amax already known (*nparts_dev partials
 // from a producer GEMM): quantises x * s to codes + native scales and computes
 // u = A(x) in one read of x; writes ts and, like launch_quant, B'.
-cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank, int parts,
                               int a_box_rows, const float* pqs, const float* partials, const int* nparts_dev,
                               void* codes, void* scales, float* ts_out, void* u, uint32_t* status,
                               const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,

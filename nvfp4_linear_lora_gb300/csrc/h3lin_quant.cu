@@ -390,11 +390,12 @@ struct QuantPassOut {
 template <bool QUANT>
 __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a, int M, int K,
-    int rank, int a_box_rows, const float* __restrict__ pqs, float* __restrict__ partials,
+    int rank, int parts, int a_box_rows, const float* __restrict__ pqs, float* __restrict__ partials,
     __nv_bfloat16* __restrict__ u, uint32_t* __restrict__ status, int stages, int tmem_cols, QuantPassOut qo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stage_bytes = 16384 + rank * 128;
+  const int pr = rank / parts;   // rank columns of u one work item computes
+  const int stage_bytes = 16384 + pr * 128;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
   uint64_t* empty = full + stages;
   uint64_t* tmem_full = empty + stages;
@@ -440,6 +441,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, status};
   const int tiles = (M + 127) >> 7;
+  const int items = tiles * parts;   // work item w: row tile w / parts, rank part w % parts
   const int nk = K >> 6;
   float ts = 1.0f;
   if (QUANT) {
@@ -460,15 +462,16 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
       uint32_t filled = 0, fill_par = 0;
       int st = 0;
       uint32_t ph = 0;
-      const uint32_t tx = 16384u + static_cast<uint32_t>(rank) * 128u;
-      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const uint32_t tx = 16384u + static_cast<uint32_t>(pr) * 128u;
+      for (int w = blockIdx.x; w < items; w += gridDim.x) {
+        const int t = w / parts, rpart = w - t * parts;
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
           uint8_t* base = smem + st * stage_bytes;
           mbar_arrive_expect_tx(&full[st], tx);
           tma_load_2d(base, &tm_x, &full[st], kc * 64, t * 128);
-          for (int rb = 0; rb < rank; rb += a_box_rows)
-            tma_load_2d(base + 16384 + rb * 128, &tm_a, &full[st], kc * 64, rb);
+          for (int rb = 0; rb < pr; rb += a_box_rows)
+            tma_load_2d(base + 16384 + rb * 128, &tm_a, &full[st], kc * 64, rpart * pr + rb);
           filled |= 1u << st;
           fill_par = (fill_par & ~(1u << st)) | (ph << st);
           if (++st == stages) { st = 0; ph ^= 1; }
@@ -482,10 +485,10 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     if (lane == 0) {
       int st = 0;
       uint32_t ph = 0, acc_ph = 0;
-      const int n_pieces = rank <= 256 ? 1 : 2;
-      const int piece_n = rank / n_pieces;
+      const int n_pieces = pr <= 256 ? 1 : 2;
+      const int piece_n = pr / n_pieces;
       const uint32_t idesc = idesc_bf16(static_cast<uint32_t>(piece_n));
-      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      for (int w = blockIdx.x; w < items; w += gridDim.x) {
         if (!mbar_wait(tmem_empty, acc_ph ^ 1, ab)) goto mma_done;
         tc_fence_after();
         for (int kc = 0; kc < nk; ++kc) {
@@ -519,8 +522,8 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     const int ch = at & 7;                   // 16-byte column chunk
     const int rb = at >> 3;                  // first row
     const int q = warp & 3;
-    const int part = aw >> 2;                // 0 .. kWorkers / 4 - 1
-    constexpr int kParts = kWorkers / 4;
+    const int cpart = aw >> 2;               // 0 .. kWorkers / 4 - 1: this warp's u column chunks
+    constexpr int kCParts = kWorkers / 4;
     float m = 0.0f;
     int st = 0;
     uint32_t ph = 0, acc_ph = 0;
@@ -547,7 +550,9 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
       load_scale8(pqs, ch, s0);
       load_scale8(pqs, (nk > 1 ? 1 : 0) * 8 + ch, s1);
     }
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+    for (int w = blockIdx.x; w < items; w += gridDim.x) {
+      const int t = w / parts, rpart = w - t * parts;
+      const bool first = rpart == 0;   // the amax / quantisation of a tile is done by its first rank part only
       // QUANT: the tile's scale atoms start at sf_tile (one per 64 columns);
       // row h's codes at code_row[h] (null past M: rows >= M get no codes)
       uint8_t* sf_tile = nullptr;
@@ -578,7 +583,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
             const uint4 w0 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj) ^ (r & 7)) << 4));
             const uint4 w1 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj + 1) ^ (r & 7)) << 4));
             // rows >= M were filled with zeros by the TMA load: scale 0, no codes
-            if (in_bounds((t * 128 + 128 <= ((M + 127) & ~127)) && 4 * kc + 3 < (K >> 4), status))
+            if (first && in_bounds((t * 128 + 128 <= ((M + 127) & ~127)) && 4 * kc + 3 < (K >> 4), status))
               quant_block(qc, code_row[h] ? code_row[h] + 4 * kc : nullptr, sf_tile + kc * 512 + sf_in_atom[h], w0,
                           w1, qs);
           }
@@ -598,14 +603,16 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
           s1[i] = s2[i];
         }
         if (!mbar_wait(&full[st], ph, ab)) goto amax_done;
-        const uint8_t* tile = smem + st * stage_bytes;
-        ColMax8 cm;
+        if (first) {
+          const uint8_t* tile = smem + st * stage_bytes;
+          ColMax8 cm;
 #pragma unroll
-        for (int i = 0; i < 128 / kLoraRowStride; ++i) {
-          const int r = rb + kLoraRowStride * i;
-          cm.add(*reinterpret_cast<const uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4)));
+          for (int i = 0; i < 128 / kLoraRowStride; ++i) {
+            const int r = rb + kLoraRowStride * i;
+            cm.add(*reinterpret_cast<const uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4)));
+          }
+          m = fmaxf(m, cm.scaled_max(s));
         }
-        m = fmaxf(m, cm.scaled_max(s));
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         if (++st == stages) { st = 0; ph ^= 1; }
@@ -616,13 +623,13 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
       {
         const int row = t * 128 + 32 * q + lane;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        for (int c0 = 32 * part; c0 < rank; c0 += 32 * kParts) {
+        for (int c0 = 32 * cpart; c0 < pr; c0 += 32 * kCParts) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           tmem_ld_wait();
-          const int nvec = (rank - c0) >= 32 ? 4 : 2;
-          if (row < M && in_bounds(row >= 0 && c0 + 8 * nvec <= rank, status)) {
-            uint4* dst = reinterpret_cast<uint4*>(u + static_cast<int64_t>(row) * rank + c0);
+          const int nvec = (pr - c0) >= 32 ? 4 : 2;
+          if (row < M && in_bounds(row >= 0 && rpart * pr + c0 + 8 * nvec <= rank, status)) {
+            uint4* dst = reinterpret_cast<uint4*>(u + static_cast<int64_t>(row) * rank + rpart * pr + c0);
             for (int v = 0; v < nvec; ++v) {
               float f[8];
 #pragma unroll
@@ -726,16 +733,42 @@ cudaError_t launch_quant(const void* x, int M, int K, const float* pqs, const fl
   return cudaGetLastError();
 }
 
+// Rank parts of the LoRA-down passes: a row tile's u = A(x) is split into
+// `parts` column ranges computed by separate CTAs, each staging the same x
+// tile (each element's sum over K runs as before, so u is the same bit for
+// bit), so that small M still fills the GPU.  Only below half a tile per SM:
+// each part re-reads x, which costs more than it gains once the tiles alone
+// come near one per SM (measured at M = 16384, 128 tiles: 0.114 -> 0.133 ms
+// for rank 384 in two parts).  Then the smallest split whose work items
+// reach one per SM, each part a multiple of 16 columns and at least 32.
+int lora_rank_parts(int64_t M, int rank, int sm_count) {
+  const int64_t tiles = (M + 127) / 128;
+  if (2 * tiles > sm_count) return 1;
+  int best = 1;
+  for (int p : {1, 2, 3, 4, 6}) {
+    if (rank % p != 0 || (rank / p) % 16 != 0 || rank / p < 32) continue;
+    best = p;
+    if (tiles * p >= sm_count) break;
+  }
+  return best;
+}
+int lora_a_box_rows(int rank, int parts) {
+  const int pr = rank / parts;
+  return pr <= 256 ? pr : pr / 2;
+}
+
 template <bool QUANT>
 static cudaError_t launch_lora_pass(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
-                                    int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
-                                    int sm_count, const QuantPassOut& qo, int* grid_out, cudaStream_t st) {
-  const int stage_bytes = 16384 + rank * 128;
+                                    int parts, int a_box_rows, const float* pqs, float* partials, void* u,
+                                    uint32_t* status, int sm_count, const QuantPassOut& qo, int* grid_out,
+                                    cudaStream_t st) {
+  const int pr = rank / parts;
+  const int stage_bytes = 16384 + pr * 128;
   constexpr int kSmemLimit = 232448;     // per CTA, one CTA per SM
   constexpr int kSmemPerSm = 233472;     // shared memory of an SM (228 KB), 1 KB of it reserved per CTA
   const int tail = 256 + (QUANT ? 2048 : 0);   // barriers, flags, partial maxima (+ bracket table)
   int tmem_cols = 32;
-  while (tmem_cols < rank) tmem_cols <<= 1;
+  while (tmem_cols < pr) tmem_cols <<= 1;
   // two CTAs per SM when their accumulators fit TMEM together and each gets a
   // ring of at least 3 stages; else one CTA with up to 8 stages
   const int two_stages = (kSmemPerSm / 2 - 1024 - 1024 - tail) / stage_bytes;
@@ -744,37 +777,39 @@ static cudaError_t launch_lora_pass(const CUtensorMap& tm_x, const CUtensorMap& 
   if (stages > 8) stages = 8;
   if (stages < 2) return cudaErrorInvalidValue;
   const int smem = stages * stage_bytes + 1024 + tail;
-  const int tiles = (M + 127) / 128;
+  const int items = (M + 127) / 128 * parts;
   const int slots = (two ? 2 : 1) * sm_count;
-  int grid = tiles < slots ? tiles : slots;
+  int grid = items < slots ? items : slots;
   if (grid > kMaxPartials) grid = kMaxPartials;
   cudaError_t e = cudaFuncSetAttribute(k_amax_lora<QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   trace_launch(QUANT ? "k_amax_lora<quant>" : "k_amax_lora<amax>", grid, 1, lora_threads<QUANT>(), smem,
-               "M=%d K=%d rank=%d stages=%d ctas_per_sm=%d tmem_cols=%d", M, K, rank, stages, two ? 2 : 1, tmem_cols);
-  k_amax_lora<QUANT><<<grid, lora_threads<QUANT>(), smem, st>>>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, partials,
+               "M=%d K=%d rank=%d rank_parts=%d stages=%d ctas_per_sm=%d tmem_cols=%d", M, K, rank, parts, stages,
+               two ? 2 : 1, tmem_cols);
+  k_amax_lora<QUANT><<<grid, lora_threads<QUANT>(), smem, st>>>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs,
+                                                                partials,
                                                        static_cast<__nv_bfloat16*>(u), status, stages, tmem_cols, qo);
   if (grid_out) *grid_out = grid;
   return cudaGetLastError();
 }
 
-cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank, int parts,
                              int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
                              int sm_count, int* nparts, cudaStream_t st) {
   QuantPassOut qo{};
-  return launch_lora_pass<false>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, partials, u, status, sm_count, qo, nparts,
-                                 st);
+  return launch_lora_pass<false>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, partials, u, status, sm_count, qo,
+                                 nparts, st);
 }
 
-cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
+cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank, int parts,
                               int a_box_rows, const float* pqs, const float* partials, const int* nparts_dev,
                               void* codes, void* scales, float* ts_out, void* u, uint32_t* status,
                               const void* b_src, void* b_dst, int64_t b_elems, float lora_k, const float* ts_w,
                               int sm_count, cudaStream_t st) {
   QuantPassOut qo{partials, nparts_dev, static_cast<uint2*>(codes), static_cast<uint8_t*>(scales), ts_out,
                   static_cast<const uint4*>(b_src), static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w};
-  return launch_lora_pass<true>(tm_x, tm_a, M, K, rank, a_box_rows, pqs, nullptr, u, status, sm_count, qo, nullptr,
-                                st);
+  return launch_lora_pass<true>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, nullptr, u, status, sm_count, qo,
+                                nullptr, st);
 }
 
 }  // namespace h3lin

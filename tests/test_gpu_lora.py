@@ -15,7 +15,9 @@ could miss LoRA errors of several percent.  These tests isolate it:
 * u = A(x), the bf16 intermediate the amax pass leaves in the workspace,
   against the oracle's t = x A^T within the bf16 rounding plus the FP32
   accumulation bound (rank 384 takes the two-piece MMA path); the
-  quantising pass of the MLP's down projection leaves the same u bit for bit;
+  quantising pass of the MLP's down projection leaves the same u bit for bit,
+  and so does a call with few rows, whose tiles split their rank columns
+  over several CTAs;
 * inputs of tiny magnitude (x ~ 2^-100, W ~ 2^-60 and others), where the
   scaled copy of B would leave the bf16 range and ts_x * ts_w underflows in
   float32: codes stay bit-exact and the output meets the bar."""
@@ -152,6 +154,24 @@ def test_u_is_A_of_x_within_bf16_rounding(M, K, N, rank):
     assert np.all(err <= bound), f"max excess {np.max(err - bound):.3e}"
     # and it is not trivially satisfied: u carries t to bf16 precision
     assert np.linalg.norm(u - t) / np.linalg.norm(t) < 2.0 ** -8
+
+
+@pytest.mark.parametrize("rank", [384, 128])
+def test_u_rows_do_not_depend_on_M(rank):
+    # below one 128-row tile per SM the LoRA-down pass splits each tile's rank
+    # columns over several CTAs (same staged x, same order over K): the rows
+    # of u must come out bit for bit as in a call with enough rows for no split
+    M_big, M_small, K = 19456, 1000, 1024
+    p = synth.projection(9300 + rank, M_big, K, 1536, rank, outlier_frac=0.01)
+    x, s, pw, ad = _dev(p)
+    us = []
+    for M in (M_big, M_small):
+        ws = h3lin.new_workspace(h3lin.h3lin_forward_workspace_bytes(M, K, 1536, rank))
+        h3lin.forward(x[:M], pw, s, ad, 1.0, workspace=ws, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert h3lin.read_status(ws) == 0
+        us.append(_u_region(ws, M, K, 1536, rank).clone())
+    assert torch.equal(us[1].view(torch.int16), us[0][:M_small].view(torch.int16))
 
 
 def test_quantising_pass_of_the_mlp_leaves_the_same_u():
