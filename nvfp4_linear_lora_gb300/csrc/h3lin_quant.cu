@@ -358,17 +358,21 @@ __global__ void __launch_bounds__(kQuantThreads, 4) k_quant(
 // Amax thread a owns the 16-byte column chunk a % 8 of rows a / 8 + R i
 // (R = 32 * warps / 8) of every stage, so its 8 per-channel scales are two
 // loads per stage.
-constexpr int kLoraAmaxWarps = 8;
-constexpr int kLoraRowStride = 32 * kLoraAmaxWarps / 8;   // rows between a thread's rows
-static_assert(128 % kLoraRowStride == 0, "rows of a tile per amax thread");
+constexpr int kLoraAmaxWarps = 8;   // per 128 rows of the tile
 // Worker warps per CTA of the quantising variant.  Two CTAs share an SM when
 // the TMEM accumulator and the ring fit twice (rank <= 256): each CTA's
 // pipeline (ring fill, tile epilogue, stalls) then overlaps the other's, which
 // measured faster than one CTA with twice the workers.
-constexpr int kLoraQuantWarps = 8;
+constexpr int kLoraQuantWarps = 8;   // per 128 rows of the tile
 constexpr bool kLoraAmaxTwoCtas = true;   // the amax pass takes two CTAs per SM as well
-template <bool QUANT> constexpr int lora_workers() { return QUANT ? kLoraQuantWarps : kLoraAmaxWarps; }
-template <bool QUANT> constexpr int lora_threads() { return 64 + 32 * lora_workers<QUANT>(); }
+// ROWS: rows of x per tile, 128 or 256.  A 256-row tile (one CTA per SM, two
+// 128-row accumulators, twice the workers) stages 32 KB of x against one
+// A slice per K step, so an SM holds a third more of x in flight than two
+// CTAs of 128-row tiles; it needs 2 * (rank / parts) <= 256 TMEM columns.
+template <bool QUANT, int ROWS> constexpr int lora_workers() {
+  return (QUANT ? kLoraQuantWarps : kLoraAmaxWarps) * (ROWS / 128);
+}
+template <bool QUANT, int ROWS> constexpr int lora_threads() { return 64 + 32 * lora_workers<QUANT, ROWS>(); }
 
 // QUANT: the amax is known (partials_in, *nparts_dev of them, left by a
 // producer GEMM), so warps 2-17 quantise the staged tile instead: thread a
@@ -387,15 +391,17 @@ struct QuantPassOut {
   const float* ts_w;
 };
 
-template <bool QUANT>
-__global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
+template <bool QUANT, int ROWS>
+__global__ void __launch_bounds__(lora_threads<QUANT, ROWS>(), ROWS == 128 ? 2 : 1) k_amax_lora(
     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a, int M, int K,
     int rank, int parts, int a_box_rows, const float* __restrict__ pqs, float* __restrict__ partials,
     __nv_bfloat16* __restrict__ u, uint32_t* __restrict__ status, int stages, int tmem_cols, QuantPassOut qo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  static_assert(ROWS == 128 || ROWS == 256, "tile rows");
+  constexpr int kXBytes = ROWS * 128;   // x tile of a stage: ROWS x 64 bf16
   const int pr = rank / parts;   // rank columns of u one work item computes
-  const int stage_bytes = 16384 + pr * 128;
+  const int stage_bytes = kXBytes + pr * 128;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
   uint64_t* empty = full + stages;
   uint64_t* tmem_full = empty + stages;
@@ -406,8 +412,8 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
   float* red = reinterpret_cast<float*>(abort_flag + 1);
   float2* yt = reinterpret_cast<float2*>(smem + stages * stage_bytes + 256);   // QUANT: 256 brackets of 1 / d
 
-  constexpr int kWorkers = lora_workers<QUANT>();
-  constexpr int kThreads = lora_threads<QUANT>();
+  constexpr int kWorkers = lora_workers<QUANT, ROWS>();
+  constexpr int kThreads = lora_threads<QUANT, ROWS>();
   const int warp = warp_id(), lane = lane_id();
   if (QUANT) {   // tensor amax from the producer's partials (every CTA, deterministic)
     const int n = min(max(*qo.nparts_dev, 0), kMaxPartials);   // never read past the partials
@@ -440,7 +446,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, status};
-  const int tiles = (M + 127) >> 7;
+  const int tiles = (M + ROWS - 1) / ROWS;
   const int items = tiles * parts;   // work item w: row tile w / parts, rank part w % parts
   const int nk = K >> 6;
   float ts = 1.0f;
@@ -462,16 +468,18 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
       uint32_t filled = 0, fill_par = 0;
       int st = 0;
       uint32_t ph = 0;
-      const uint32_t tx = 16384u + static_cast<uint32_t>(pr) * 128u;
+      const uint32_t tx = static_cast<uint32_t>(kXBytes) + static_cast<uint32_t>(pr) * 128u;
       for (int w = blockIdx.x; w < items; w += gridDim.x) {
         const int t = w / parts, rpart = w - t * parts;
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait(&empty[st], ph ^ 1, ab)) goto producer_done;
           uint8_t* base = smem + st * stage_bytes;
           mbar_arrive_expect_tx(&full[st], tx);
-          tma_load_2d(base, &tm_x, &full[st], kc * 64, t * 128);
+#pragma unroll
+          for (int hh = 0; hh < ROWS / 128; ++hh)
+            tma_load_2d(base + hh * 16384, &tm_x, &full[st], kc * 64, t * ROWS + hh * 128);
           for (int rb = 0; rb < pr; rb += a_box_rows)
-            tma_load_2d(base + 16384 + rb * 128, &tm_a, &full[st], kc * 64, rpart * pr + rb);
+            tma_load_2d(base + kXBytes + rb * 128, &tm_a, &full[st], kc * 64, rpart * pr + rb);
           filled |= 1u << st;
           fill_par = (fill_par & ~(1u << st)) | (ph << st);
           if (++st == stages) { st = 0; ph ^= 1; }
@@ -495,13 +503,16 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
           if (!mbar_wait(&full[st], ph, ab)) goto mma_done;
           tc_fence_after();
           const uint32_t xa = smem_u32(smem + st * stage_bytes);
-          const uint32_t aa = xa + 16384u;
+          const uint32_t aa = xa + static_cast<uint32_t>(kXBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = sdesc_kmajor_sw128(xa + kk * 32);
-            for (int p = 0; p < n_pieces; ++p) {
-              const uint64_t bdesc = sdesc_kmajor_sw128(aa + p * piece_n * 128 + kk * 32);
-              mma_bf16(tmem + p * piece_n, adesc, bdesc, idesc, (kc | kk) != 0);
+#pragma unroll
+            for (int hh = 0; hh < ROWS / 128; ++hh) {   // rows 128 hh ..: accumulator at column hh * pr
+              const uint64_t adesc = sdesc_kmajor_sw128(xa + hh * 16384 + kk * 32);
+              for (int p = 0; p < n_pieces; ++p) {
+                const uint64_t bdesc = sdesc_kmajor_sw128(aa + p * piece_n * 128 + kk * 32);
+                mma_bf16(tmem + hh * pr + p * piece_n, adesc, bdesc, idesc, (kc | kk) != 0);
+              }
             }
           }
           tc_commit(&empty[st]);
@@ -531,16 +542,11 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     // scales are loaded one stage ahead
     const int qj = at & 3, qr = at >> 2;
     const QuantCtx qc = make_quant_ctx(ts, yt);
-    constexpr int kQuantRowStep = 8 * kWorkers;       // rows covered by the workers at once
-    constexpr int kQuantRows = 128 / kQuantRowStep;   // rows of a tile per thread
-    // byte offset of block qj of each of this thread's rows inside a 512-byte
-    // scale atom (the native layout: (r % 32) * 16 + (r / 32) * 4 + j)
-    int sf_in_atom[kQuantRows];
-#pragma unroll
-    for (int h = 0; h < kQuantRows; ++h) {
-      const int r = qr + kQuantRowStep * h;
-      sf_in_atom[h] = (r & 31) * 16 + (r >> 5) * 4 + qj;
-    }
+    constexpr int kQuantRowStep = 8 * kWorkers;        // rows covered by the workers at once
+    constexpr int kQuantRows = ROWS / kQuantRowStep;   // rows of a tile per thread
+    static_assert(kQuantRows * kQuantRowStep == ROWS, "rows of a tile per quantising thread");
+    constexpr int kRowStride = 32 * kWorkers / 8;      // amax: rows between a thread's rows
+    static_assert(ROWS % kRowStride == 0, "rows of a tile per amax thread");
     float qs_next[16];
     if (QUANT) load_scale16(pqs, qj, qs_next);
     // The per-channel scales of a stage are loaded two stages ahead: the
@@ -553,15 +559,21 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
     for (int w = blockIdx.x; w < items; w += gridDim.x) {
       const int t = w / parts, rpart = w - t * parts;
       const bool first = rpart == 0;   // the amax / quantisation of a tile is done by its first rank part only
-      // QUANT: the tile's scale atoms start at sf_tile (one per 64 columns);
-      // row h's codes at code_row[h] (null past M: rows >= M get no codes)
-      uint8_t* sf_tile = nullptr;
+      // QUANT: row h's scale byte of the stage's first 64 columns at sf_row[h]
+      // (the native layout: 512-byte atoms of 128 rows x 64 columns ordered
+      // [rows / 128][K / 64], (r % 32) * 16 + (r % 128 / 32) * 4 + j inside;
+      // null past the scales' 128-row padding), its codes at code_row[h]
+      // (null past M: rows >= M get no codes)
+      uint8_t* sf_row[kQuantRows];
       uint2* code_row[kQuantRows];
       if (QUANT) {
-        sf_tile = qo.scales + static_cast<int64_t>(t) * (K >> 6) * 512;
 #pragma unroll
         for (int h = 0; h < kQuantRows; ++h) {
-          const int row = t * 128 + qr + kQuantRowStep * h;
+          const int row = t * ROWS + qr + kQuantRowStep * h;
+          sf_row[h] = row < ((M + 127) & ~127)
+                          ? qo.scales + static_cast<int64_t>(row >> 7) * (K >> 6) * 512 + (row & 31) * 16 +
+                                ((row & 127) >> 5) * 4 + qj
+                          : nullptr;
           code_row[h] = row < M ? qo.codes + static_cast<int64_t>(row) * (K >> 4) + qj : nullptr;
         }
       }
@@ -583,9 +595,8 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
             const uint4 w0 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj) ^ (r & 7)) << 4));
             const uint4 w1 = *reinterpret_cast<const uint4*>(tile + r * 128 + (((2 * qj + 1) ^ (r & 7)) << 4));
             // rows >= M were filled with zeros by the TMA load: scale 0, no codes
-            if (first && in_bounds((t * 128 + 128 <= ((M + 127) & ~127)) && 4 * kc + 3 < (K >> 4), status))
-              quant_block(qc, code_row[h] ? code_row[h] + 4 * kc : nullptr, sf_tile + kc * 512 + sf_in_atom[h], w0,
-                          w1, qs);
+            if (first && sf_row[h] && in_bounds(4 * kc + 3 < (K >> 4), status))
+              quant_block(qc, code_row[h] ? code_row[h] + 4 * kc : nullptr, sf_row[h] + kc * 512, w0, w1, qs);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[st]);
@@ -607,8 +618,8 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
           const uint8_t* tile = smem + st * stage_bytes;
           ColMax8 cm;
 #pragma unroll
-          for (int i = 0; i < 128 / kLoraRowStride; ++i) {
-            const int r = rb + kLoraRowStride * i;
+          for (int i = 0; i < ROWS / kRowStride; ++i) {
+            const int r = rb + kRowStride * i;
             cm.add(*reinterpret_cast<const uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4)));
           }
           m = fmaxf(m, cm.scaled_max(s));
@@ -620,9 +631,10 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
       // epilogue: u[row, :] = bf16(acc * u_mul) (u_mul = 1 but for tiny tensor scales)
       if (!mbar_wait(tmem_full, acc_ph, ab)) goto amax_done;
       tc_fence_after();
-      {
-        const int row = t * 128 + 32 * q + lane;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+#pragma unroll 1
+      for (int hh = 0; hh < ROWS / 128; ++hh) {   // rows 128 hh ..: accumulator at column hh * pr
+        const int row = t * ROWS + hh * 128 + 32 * q + lane;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + hh * pr;
         for (int c0 = 32 * cpart; c0 < pr; c0 += 32 * kCParts) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
@@ -663,7 +675,7 @@ __global__ void __launch_bounds__(lora_threads<QUANT>(), 2) k_amax_lora(
   __syncthreads();
   if (!QUANT && threadIdx.x == 0 && in_bounds(blockIdx.x < static_cast<unsigned>(kMaxPartials), status)) {
     float m = red[0];
-    for (int i = 1; i < kLoraAmaxWarps; ++i) m = fmaxf(m, red[i]);
+    for (int i = 1; i < kWorkers; ++i) m = fmaxf(m, red[i]);
     partials[blockIdx.x] = m;
   }
   if (warp == 1) {
@@ -757,48 +769,61 @@ int lora_a_box_rows(int rank, int parts) {
   return pr <= 256 ? pr : pr / 2;
 }
 
-template <bool QUANT>
+template <bool QUANT, int ROWS>
 static cudaError_t launch_lora_pass(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank,
                                     int parts, int a_box_rows, const float* pqs, float* partials, void* u,
                                     uint32_t* status, int sm_count, const QuantPassOut& qo, int* grid_out,
                                     cudaStream_t st) {
   const int pr = rank / parts;
-  const int stage_bytes = 16384 + pr * 128;
+  const int stage_bytes = ROWS * 128 + pr * 128;
   constexpr int kSmemLimit = 232448;     // per CTA, one CTA per SM
   constexpr int kSmemPerSm = 233472;     // shared memory of an SM (228 KB), 1 KB of it reserved per CTA
   const int tail = 256 + (QUANT ? 2048 : 0);   // barriers, flags, partial maxima (+ bracket table)
   int tmem_cols = 32;
-  while (tmem_cols < pr) tmem_cols <<= 1;
-  // two CTAs per SM when their accumulators fit TMEM together and each gets a
-  // ring of at least 3 stages; else one CTA with up to 8 stages
+  while (tmem_cols < (ROWS / 128) * pr) tmem_cols <<= 1;
+  // 128-row tiles: two CTAs per SM when their accumulators fit TMEM together
+  // and each gets a ring of at least 3 stages; else (and for 256-row tiles)
+  // one CTA with up to 8 stages
   const int two_stages = (kSmemPerSm / 2 - 1024 - 1024 - tail) / stage_bytes;
-  const bool two = (QUANT || kLoraAmaxTwoCtas) && 2 * tmem_cols <= 512 && two_stages >= 3;
+  const bool two = ROWS == 128 && (QUANT || kLoraAmaxTwoCtas) && 2 * tmem_cols <= 512 && two_stages >= 3;
   int stages = two ? two_stages : (kSmemLimit - 1024 - tail) / stage_bytes;
   if (stages > 8) stages = 8;
   if (stages < 2) return cudaErrorInvalidValue;
   const int smem = stages * stage_bytes + 1024 + tail;
-  const int items = (M + 127) / 128 * parts;
+  const int items = (M + ROWS - 1) / ROWS * parts;
   const int slots = (two ? 2 : 1) * sm_count;
   int grid = items < slots ? items : slots;
   if (grid > kMaxPartials) grid = kMaxPartials;
-  cudaError_t e = cudaFuncSetAttribute(k_amax_lora<QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = k_amax_lora<QUANT, ROWS>;
+  constexpr int kThreads = lora_threads<QUANT, ROWS>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  trace_launch(QUANT ? "k_amax_lora<quant>" : "k_amax_lora<amax>", grid, 1, lora_threads<QUANT>(), smem,
-               "M=%d K=%d rank=%d rank_parts=%d stages=%d ctas_per_sm=%d tmem_cols=%d", M, K, rank, parts, stages,
-               two ? 2 : 1, tmem_cols);
-  k_amax_lora<QUANT><<<grid, lora_threads<QUANT>(), smem, st>>>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs,
-                                                                partials,
-                                                       static_cast<__nv_bfloat16*>(u), status, stages, tmem_cols, qo);
+  trace_launch(QUANT ? "k_amax_lora<quant>" : "k_amax_lora<amax>", grid, 1, kThreads, smem,
+               "M=%d K=%d rank=%d rank_parts=%d tile_rows=%d stages=%d ctas_per_sm=%d tmem_cols=%d", M, K, rank,
+               parts, ROWS, stages, two ? 2 : 1, tmem_cols);
+  kern<<<grid, kThreads, smem, st>>>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, partials,
+                                     static_cast<__nv_bfloat16*>(u), status, stages, tmem_cols, qo);
   if (grid_out) *grid_out = grid;
   return cudaGetLastError();
+}
+
+// Tile rows of the LoRA-down passes: 256 when two 128-row accumulators of
+// rank / parts columns fit TMEM and the 256-row tiles still give about one
+// per SM, else 128.
+static int lora_tile_rows(int64_t M, int rank, int parts, int sm_count) {
+  const int64_t tiles256 = (M + 255) / 256 * parts;
+  return (rank / parts <= 128 && 4 * tiles256 >= 3 * int64_t(sm_count)) ? 256 : 128;
 }
 
 cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank, int parts,
                              int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
                              int sm_count, int* nparts, cudaStream_t st) {
   QuantPassOut qo{};
-  return launch_lora_pass<false>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, partials, u, status, sm_count, qo,
-                                 nparts, st);
+  if (lora_tile_rows(M, rank, parts, sm_count) == 256)
+    return launch_lora_pass<false, 256>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, partials, u, status,
+                                        sm_count, qo, nparts, st);
+  return launch_lora_pass<false, 128>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, partials, u, status, sm_count,
+                                      qo, nparts, st);
 }
 
 cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank, int parts,
@@ -808,8 +833,11 @@ cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, 
                               int sm_count, cudaStream_t st) {
   QuantPassOut qo{partials, nparts_dev, static_cast<uint2*>(codes), static_cast<uint8_t*>(scales), ts_out,
                   static_cast<const uint4*>(b_src), static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w};
-  return launch_lora_pass<true>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, nullptr, u, status, sm_count, qo,
-                                nullptr, st);
+  if (lora_tile_rows(M, rank, parts, sm_count) == 256)
+    return launch_lora_pass<true, 256>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, nullptr, u, status, sm_count,
+                                       qo, nullptr, st);
+  return launch_lora_pass<true, 128>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, nullptr, u, status, sm_count,
+                                     qo, nullptr, st);
 }
 
 }  // namespace h3lin

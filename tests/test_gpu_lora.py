@@ -156,12 +156,14 @@ def test_u_is_A_of_x_within_bf16_rounding(M, K, N, rank):
     assert np.linalg.norm(u - t) / np.linalg.norm(t) < 2.0 ** -8
 
 
-@pytest.mark.parametrize("rank", [384, 128])
-def test_u_rows_do_not_depend_on_M(rank):
-    # below one 128-row tile per SM the LoRA-down pass splits each tile's rank
-    # columns over several CTAs (same staged x, same order over K): the rows
-    # of u must come out bit for bit as in a call with enough rows for no split
-    M_big, M_small, K = 19456, 1000, 1024
+@pytest.mark.parametrize("rank,M_big,M_small", [(384, 19456, 1000), (128, 19456, 1000), (128, 37726, 19456)])
+def test_u_rows_do_not_depend_on_M(rank, M_big, M_small):
+    # the LoRA-down pass picks its work split by M: below one 128-row tile per
+    # SM each tile's rank columns go to several CTAs; with enough rows (and
+    # rank <= 128) a CTA takes 256-row tiles with two accumulators.  Either way
+    # every u element is the same sum over K, so the rows of u must come out
+    # bit for bit as in a call of another size
+    K = 1024
     p = synth.projection(9300 + rank, M_big, K, 1536, rank, outlier_frac=0.01)
     x, s, pw, ad = _dev(p)
     us = []
