@@ -807,21 +807,20 @@ static cudaError_t launch_lora_pass(const CUtensorMap& tm_x, const CUtensorMap& 
   return cudaGetLastError();
 }
 
-// Tile rows of the LoRA-down passes: 256 when two 128-row accumulators of
-// rank / parts columns fit TMEM and the 256-row tiles still give about one
-// per SM, else 128.
-static int lora_tile_rows(int64_t M, int rank, int parts, int sm_count) {
+// Tile rows of the LoRA-down passes.  The quantising pass takes 256 when two
+// 128-row accumulators of rank / parts columns fit TMEM and the 256-row tiles
+// still give about one per SM (down at S = 37726: 358 -> 284 us); the amax
+// pass keeps 128 (its two CTAs per SM already stream x at 86 % of HBM, and
+// 256-row tiles measured 66 -> 76 us there).
+static int lora_tile_rows(bool quant, int64_t M, int rank, int parts, int sm_count) {
   const int64_t tiles256 = (M + 255) / 256 * parts;
-  return (rank / parts <= 128 && 4 * tiles256 >= 3 * int64_t(sm_count)) ? 256 : 128;
+  return (quant && rank / parts <= 128 && 4 * tiles256 >= 3 * int64_t(sm_count)) ? 256 : 128;
 }
 
 cudaError_t launch_amax_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, int M, int K, int rank, int parts,
                              int a_box_rows, const float* pqs, float* partials, void* u, uint32_t* status,
                              int sm_count, int* nparts, cudaStream_t st) {
   QuantPassOut qo{};
-  if (lora_tile_rows(M, rank, parts, sm_count) == 256)
-    return launch_lora_pass<false, 256>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, partials, u, status,
-                                        sm_count, qo, nparts, st);
   return launch_lora_pass<false, 128>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, partials, u, status, sm_count,
                                       qo, nparts, st);
 }
@@ -833,7 +832,7 @@ cudaError_t launch_quant_lora(const CUtensorMap& tm_x, const CUtensorMap& tm_a, 
                               int sm_count, cudaStream_t st) {
   QuantPassOut qo{partials, nparts_dev, static_cast<uint2*>(codes), static_cast<uint8_t*>(scales), ts_out,
                   static_cast<const uint4*>(b_src), static_cast<uint4*>(b_dst), b_elems / 8, lora_k, ts_w};
-  if (lora_tile_rows(M, rank, parts, sm_count) == 256)
+  if (lora_tile_rows(true, M, rank, parts, sm_count) == 256)
     return launch_lora_pass<true, 256>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, nullptr, u, status, sm_count,
                                        qo, nullptr, st);
   return launch_lora_pass<true, 128>(tm_x, tm_a, M, K, rank, parts, a_box_rows, pqs, nullptr, u, status, sm_count,
