@@ -14,7 +14,8 @@ could miss LoRA errors of several percent.  These tests isolate it:
   branch's bf16 intermediates and FP32 sums allow;
 * u = A(x), the bf16 intermediate the amax pass leaves in the workspace,
   against the oracle's t = x A^T within the bf16 rounding plus the FP32
-  accumulation bound (rank 384 takes the two-piece MMA path); the
+  accumulation bound (rank 384 takes the two-piece MMA path, with its rank
+  columns split over CTAs below half a 128-row tile per SM); the
   quantising pass of the MLP's down projection leaves the same u bit for bit,
   and so does a call with few rows, whose tiles split their rank columns
   over several CTAs;
@@ -139,8 +140,8 @@ def _t_bound(x, A):
     return t, 2.0 ** -8 * np.abs(t) + 2.0 * K * 2.0 ** -24 * acc
 
 
-@pytest.mark.parametrize("M,K,N,rank", [(2000, 5120, 15360, 384), (1537, 5120, 5120, 128), (300, 1024, 1280, 256),
-                                        (129, 512, 512, 16)])
+@pytest.mark.parametrize("M,K,N,rank", [(2000, 5120, 15360, 384), (9437, 5120, 15360, 384), (1537, 5120, 5120, 128),
+                                        (300, 1024, 1280, 256), (129, 512, 512, 16)])
 def test_u_is_A_of_x_within_bf16_rounding(M, K, N, rank):
     p = synth.projection(9000 + rank, M, K, N, rank, outlier_frac=0.01)
     x, s, pw, ad = _dev(p)
@@ -158,10 +159,10 @@ def test_u_is_A_of_x_within_bf16_rounding(M, K, N, rank):
 
 @pytest.mark.parametrize("rank,M_big,M_small", [(384, 19456, 1000), (128, 19456, 1000)])
 def test_u_rows_do_not_depend_on_M(rank, M_big, M_small):
-    # the LoRA-down pass picks its work split by M: below one 128-row tile per
-    # SM each tile's rank columns go to several CTAs.  Every u element is still
-    # the same sum over K, so the rows of u must come out bit for bit as in a
-    # call with enough rows for no split
+    # the LoRA-down pass picks its work split by M: below half a 128-row tile
+    # per SM each tile's rank columns go to several CTAs.  Every u element is
+    # still the same sum over K, so the rows of u must come out bit for bit as
+    # in a call with enough rows for no split
     K = 1024
     p = synth.projection(9300 + rank, M_big, K, 1536, rank, outlier_frac=0.01)
     x, s, pw, ad = _dev(p)
