@@ -87,6 +87,22 @@ def test_base_path_matches_oracle(M, K, N, rank, silu):
     assert_bf16_is_rounded_f32(p, silu=silu, use_adapter=False, dev=dev, pw=pw)
 
 
+# CTA-pair GEMM (N % 256 == 0) at the 256-row tile boundaries: a single row,
+# one row short of / exactly / one past one and two pair tiles, with and
+# without SiLU*up, LoRA ranks that leave a partial 64-wide LoRA stage.
+PAIR_EDGES = [(M, 512, 512, rank, silu) for M in (1, 255, 256, 257, 511, 512, 513)
+              for rank, silu in ((48, False), (80, True))]
+
+
+@pytest.mark.parametrize("M,K,N,rank,silu", PAIR_EDGES)
+def test_pair_tile_boundaries(M, K, N, rank, silu):
+    p = synth.projection(3000 + M + rank, M, K, N, rank, outlier_frac=0.01)
+    got, dev, pw = run(p, silu=silu)
+    assert got.shape == (M, N // 2 if silu else N)
+    assert_parity(got, ref(p, silu=silu), f"pair edge M={M} r={rank} silu={silu}")
+    assert_bf16_is_rounded_f32(p, silu=silu, dev=dev, pw=pw)
+
+
 def test_tiny_workload_matches_oracle():
     c = configs.TINY
     p = synth.projection(c["seed"], c["M"], c["K"], c["N"], c["rank"])
